@@ -1,0 +1,253 @@
+"""Seeded synthetic verify batches.
+
+This module builds inputs only: sequence lengths, draft counts, query rows and
+a paged KV cache that holds each sequence's logical K/V. It contains none of
+the attention arithmetic, so that the CUDA path and the CPU oracle can both be
+fed from it without sharing any of the method's code.
+
+Workloads (all Q/K/V drawn from N(0, 1) in fp32, then cast):
+
+  tiny            fp32, bs 2, 4 q-heads / 2 kv-heads, head dim 64, prefixes 37
+                  and 90, 4 causal drafts, page size 1, the pages a random
+                  permutation of a 256-slot pool, scale 1/8, seed 0
+  llama8b_gqa     Llama-3.1-8B-shaped GQA verify: bf16, 32 / 8 heads, head dim
+                  128, bs 16, prefixes uniform in [1024, 8192], 4 drafts, page
+                  size 4, a random page permutation over a 2M-token pool
+  long_context    bf16, 32 / 8 heads, head dim 128, bs 4, prefixes uniform in
+                  [32768, 131072], 4 drafts, page size 64
+  dsv3_mla        DeepSeek-V3-shaped absorbed MLA: bf16, 128 q-heads sharing one
+                  latent KV head, qk dim 576 (512 latent + 64 rope), v dim 512
+                  (the first 512 entries of the same row), bs 32, prefixes
+                  uniform in [2048, 16384], 3 drafts, page size 64, scale
+                  1/sqrt(192)
+  mixed_serving   bf16, 64 / 8 heads, qk dim 192, v dim 128, bs 128, prefixes
+                  lognormal (median 2048, sigma 1) clipped to [1, 65536], 2..5
+                  drafts per sequence, page size 16, sliding window 4096 on
+                  every other call
+
+Where a pool size is not given it holds 1.25x the pages the batch needs. Pool
+slots that no sequence owns, and the tail of each sequence's last page, hold
+NaN, so any read outside a sequence's own tokens shows up in the results.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: torch.dtype
+    bs: int
+    num_q_heads: int
+    num_kv_heads: int
+    qk_dim: int
+    v_dim: int
+    page_size: int
+    prefix: tuple            # ("fixed", [..]) | ("uniform", lo, hi) | ("lognormal", median, sigma, lo, hi)
+    draft: tuple             # ("fixed", d) | ("choice", [d0, d1, ..])
+    seed: int
+    scale: float
+    v_aliases_k: bool = False
+    pool_tokens: int | None = None   # None: 1.25x the pages needed
+    window: tuple = (-1,)            # window of call c is window[c % len(window)]
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    def window_for_call(self, call: int) -> int:
+        return self.window[call % len(self.window)]
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", torch.float32, 2, 4, 2, 64, 64, 1, ("fixed", [37, 90]),
+                     ("fixed", 4), 0, 1.0 / 8.0, pool_tokens=256),
+    "llama8b_gqa": Workload("llama8b_gqa", torch.bfloat16, 16, 32, 8, 128, 128, 4,
+                            ("uniform", 1024, 8192), ("fixed", 4), 1, 1.0 / math.sqrt(128),
+                            pool_tokens=1 << 21),
+    "long_context": Workload("long_context", torch.bfloat16, 4, 32, 8, 128, 128, 64,
+                             ("uniform", 32768, 131072), ("fixed", 4), 2, 1.0 / math.sqrt(128)),
+    "dsv3_mla": Workload("dsv3_mla", torch.bfloat16, 32, 128, 1, 576, 512, 64,
+                         ("uniform", 2048, 16384), ("fixed", 3), 3, 1.0 / math.sqrt(192),
+                         v_aliases_k=True),
+    "mixed_serving": Workload("mixed_serving", torch.bfloat16, 128, 64, 8, 192, 128, 16,
+                              ("lognormal", 2048.0, 1.0, 1, 65536), ("choice", [2, 3, 4, 5]), 4,
+                              1.0 / math.sqrt(192), window=(-1, 4096)),
+}
+
+
+@dataclasses.dataclass
+class Logical:
+    """A batch before paging: per-sequence lengths, queries and contiguous K/V."""
+    wl: Workload
+    seq_lens: torch.Tensor    # int32 [bs] (CPU)
+    num_draft: torch.Tensor   # int32 [bs] (CPU)
+    q: torch.Tensor           # [sum D, Hq, Dqk]
+    k: torch.Tensor           # [sum T, Hkv, Dqk], T_b = P_b + D_b, sequences back to back
+    v: torch.Tensor | None    # [sum T, Hkv, Dv] (None when V aliases K)
+    tok_off: torch.Tensor     # int64 [bs + 1] offsets of each sequence in k / v (CPU)
+
+
+@dataclasses.dataclass
+class Paged:
+    """The call's arguments: paged K/V pools and the CSR page table."""
+    wl: Workload
+    q: torch.Tensor
+    k_cache: torch.Tensor       # [num_pages, page_size, Hkv, Dqk]
+    v_cache: torch.Tensor       # [num_pages, page_size, Hkv, Dv] (k_cache itself when aliased)
+    page_table: torch.Tensor    # int32 [kv_indptr[-1]]
+    kv_indptr: torch.Tensor     # int32 [bs + 1]
+    seq_lens: torch.Tensor      # int32 [bs]
+    num_draft: torch.Tensor     # int32 [bs]
+    page_size: int
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q.shape[0])
+
+    def to(self, device) -> "Paged":
+        f = lambda t: t.to(device)
+        kc = f(self.k_cache)
+        vc = kc if self.v_cache is self.k_cache else f(self.v_cache)
+        return Paged(self.wl, f(self.q), kc, vc, f(self.page_table), f(self.kv_indptr),
+                     f(self.seq_lens), f(self.num_draft), self.page_size)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def draw_lengths(wl: Workload, seed: int | None = None):
+    """Prefix lengths P_b and draft counts D_b (int32 CPU tensors)."""
+    g = _gen(wl.seed if seed is None else seed, "cpu")
+    kind = wl.prefix[0]
+    if kind == "fixed":
+        p = torch.tensor(wl.prefix[1][: wl.bs], dtype=torch.int64)
+        if p.numel() < wl.bs:
+            p = p.repeat((wl.bs + p.numel() - 1) // p.numel())[: wl.bs]
+    elif kind == "uniform":
+        lo, hi = wl.prefix[1], wl.prefix[2]
+        p = torch.randint(lo, hi + 1, (wl.bs,), generator=g, dtype=torch.int64)
+    elif kind == "lognormal":
+        median, sigma, lo, hi = wl.prefix[1:]
+        z = torch.randn(wl.bs, generator=g, dtype=torch.float64)
+        p = torch.exp(math.log(median) + sigma * z).round().to(torch.int64).clamp(lo, hi)
+    else:
+        raise ValueError(kind)
+    if wl.draft[0] == "fixed":
+        d = torch.full((wl.bs,), wl.draft[1], dtype=torch.int64)
+    else:
+        choices = torch.tensor(wl.draft[1], dtype=torch.int64)
+        d = choices[torch.randint(0, len(choices), (wl.bs,), generator=g)]
+    return p.to(torch.int32), d.to(torch.int32)
+
+
+def make_logical(wl: Workload, device="cpu", seed: int | None = None,
+                 seq_lens=None, num_draft=None) -> Logical:
+    """Draws lengths (unless given), Q and the contiguous per-sequence K/V."""
+    seed = wl.seed if seed is None else seed
+    if seq_lens is None or num_draft is None:
+        p, d = draw_lengths(wl, seed)
+        seq_lens = p if seq_lens is None else seq_lens
+        num_draft = d if num_draft is None else num_draft
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).cpu()
+    num_draft = torch.as_tensor(num_draft, dtype=torch.int32).cpu()
+    t = seq_lens.to(torch.int64) + num_draft.to(torch.int64)
+    tok_off = torch.zeros(len(t) + 1, dtype=torch.int64)
+    tok_off[1:] = torch.cumsum(t, 0)
+    total_t, total_q = int(tok_off[-1]), int(num_draft.sum())
+    g = _gen(seed + 7919, device)
+    f32 = dict(dtype=torch.float32, device=device, generator=g)
+    q = torch.randn(total_q, wl.num_q_heads, wl.qk_dim, **f32).to(wl.dtype)
+    k = torch.randn(total_t, wl.num_kv_heads, wl.qk_dim, **f32).to(wl.dtype)
+    v = None if wl.v_aliases_k else torch.randn(total_t, wl.num_kv_heads, wl.v_dim, **f32).to(wl.dtype)
+    return Logical(wl, seq_lens, num_draft, q, k, v, tok_off)
+
+
+def paginate(lg: Logical, page_size: int | None = None, pool_pages: int | None = None,
+             seed: int | None = None, device=None) -> Paged:
+    """Scatters the logical K/V into a NaN-poisoned paged pool.
+
+    Each sequence takes ceil(T_b / page_size) pages, drawn in order from a
+    seeded random permutation of the pool's pages; its logical token j goes to
+    entry j // page_size of its page list, row j % page_size.
+    """
+    wl = lg.wl
+    ps = wl.page_size if page_size is None else page_size
+    device = lg.k.device if device is None else device
+    seed = wl.seed if seed is None else seed
+    t = (lg.seq_lens.to(torch.int64) + lg.num_draft.to(torch.int64))
+    pages_per_seq = (t + ps - 1) // ps
+    need = int(pages_per_seq.sum())
+    if pool_pages is None:
+        if wl.pool_tokens is not None and page_size in (None, wl.page_size):
+            pool_pages = wl.pool_tokens // ps
+        else:
+            pool_pages = max(1, int(math.ceil(need * 1.25)))
+    if pool_pages < need:
+        raise ValueError(f"pool of {pool_pages} pages cannot hold the {need} the batch needs")
+    perm = torch.randperm(pool_pages, generator=_gen(seed + 104729, "cpu"), dtype=torch.int64)
+    page_table = perm[:need].to(torch.int32)
+    kv_indptr = torch.zeros(len(t) + 1, dtype=torch.int32)
+    kv_indptr[1:] = torch.cumsum(pages_per_seq, 0).to(torch.int32)
+
+    # physical slot of every logical token, sequence by sequence
+    slots = []
+    for b in range(len(t)):
+        j = torch.arange(int(t[b]), dtype=torch.int64)
+        pages = page_table[int(kv_indptr[b]):int(kv_indptr[b + 1])].to(torch.int64)
+        slots.append(pages[j // ps] * ps + j % ps)
+    slots = torch.cat(slots) if slots else torch.zeros(0, dtype=torch.int64)
+    slots = slots.to(device)
+
+    hkv = wl.num_kv_heads
+    k_cache = torch.full((pool_pages, ps, hkv, wl.qk_dim), float("nan"), dtype=wl.dtype, device=device)
+    k_cache.view(-1, hkv, wl.qk_dim).index_copy_(0, slots, lg.k.to(device))
+    if wl.v_aliases_k:
+        v_cache = k_cache
+    else:
+        v_cache = torch.full((pool_pages, ps, hkv, wl.v_dim), float("nan"), dtype=wl.dtype, device=device)
+        v_cache.view(-1, hkv, wl.v_dim).index_copy_(0, slots, lg.v.to(device))
+    return Paged(wl, lg.q.to(device), k_cache, v_cache, page_table.to(device), kv_indptr.to(device),
+                 lg.seq_lens.to(device), lg.num_draft.to(device), ps)
+
+
+def make_batch(name_or_wl, device="cpu", seed: int | None = None, **overrides) -> Paged:
+    wl = WORKLOADS[name_or_wl] if isinstance(name_or_wl, str) else name_or_wl
+    if overrides:
+        wl = wl.replace(**overrides)
+    return paginate(make_logical(wl, device=device, seed=seed), seed=seed)
+
+
+def raw_bits(t: torch.Tensor):
+    """numpy view of a tensor's elements as the oracle takes them: float32, or
+    the uint16 bit patterns of a bf16 / fp16 tensor."""
+    import numpy as np
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    raise TypeError(t.dtype)
+
+
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
+def kv_token_bytes(wl: Workload) -> int:
+    """Bytes of K (+ V unless aliased) that one KV token carries across all kv-heads."""
+    e = torch.finfo(wl.dtype).bits // 8
+    return wl.num_kv_heads * (wl.qk_dim + (0 if wl.v_aliases_k else wl.v_dim)) * e

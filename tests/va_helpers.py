@@ -1,0 +1,80 @@
+"""Shared test helpers: run the oracle on a synthetic batch, dense brute force,
+and the element-wise tolerance check used by the parity tests."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+from scipy.special import logsumexp
+
+import oracle
+from speculative_decoding_verify_topk_gb300 import synth
+
+
+def oracle_on(pb: synth.Paged, window: int = -1, num_splits: int = 1, rows=None,
+              threads: int = 0, mutant: int = 0, mutant_dir=None, scale=None):
+    wl = pb.wl
+    return oracle.verify_attn(
+        synth.raw_bits(pb.q), synth.raw_bits(pb.k_cache),
+        None if wl.v_aliases_k else synth.raw_bits(pb.v_cache),
+        pb.page_table.cpu().numpy(), pb.kv_indptr.cpu().numpy(),
+        pb.seq_lens.cpu().numpy(), pb.num_draft.cpu().numpy(),
+        num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim,
+        v_dim=wl.v_dim, page_size=pb.page_size, dtype=synth.DTYPE_CODES[wl.dtype],
+        scale=wl.scale if scale is None else scale, window=window,
+        v_aliases_k=wl.v_aliases_k, num_pages=pb.num_pages, num_splits=num_splits,
+        rows=rows, threads=threads, mutant=mutant, mutant_dir=mutant_dir)
+
+
+def brute_force(lg: synth.Logical, window: int = -1, scale=None):
+    """Dense attention straight from the contiguous per-sequence K/V: the full
+    D_b x T_b score matrix with an explicit boolean mask, then a softmax."""
+    wl = lg.wl
+    scale = wl.scale if scale is None else scale
+    q = lg.q.double().cpu().numpy()
+    k = lg.k.double().cpu().numpy()
+    v = (k[..., : wl.v_dim] if wl.v_aliases_k else lg.v.double().cpu().numpy())
+    outs, lses = [], []
+    qrow = 0
+    for b in range(wl.bs):
+        p_b, d_b = int(lg.seq_lens[b]), int(lg.num_draft[b])
+        t0, t1 = int(lg.tok_off[b]), int(lg.tok_off[b + 1])
+        pos = p_b + np.arange(d_b)[:, None]          # query positions
+        key = np.arange(t1 - t0)[None, :]            # key positions
+        allowed = key <= pos
+        if window >= 0:
+            allowed &= key >= pos - window
+        o_b = np.empty((d_b, wl.num_q_heads, wl.v_dim))
+        l_b = np.empty((d_b, wl.num_q_heads))
+        for h in range(wl.num_q_heads):
+            g = h // wl.group
+            s = scale * q[qrow:qrow + d_b, h, :] @ k[t0:t1, g, :].T
+            s = np.where(allowed, s, -np.inf)
+            lse = logsumexp(s, axis=1)
+            o_b[:, h, :] = np.exp(s - lse[:, None]) @ v[t0:t1, g, :]
+            l_b[:, h] = lse
+        outs.append(o_b)
+        lses.append(l_b)
+        qrow += d_b
+    return np.concatenate(outs), np.concatenate(lses)
+
+
+def tolerance(dtype: torch.dtype):
+    """(atol, rtol, lse_atol): bf16/fp16 inputs with fp32 accumulation are held to
+    1e-2 / 1e-2 on outputs and 1e-3 on the log-sum-exp, fp32 inputs to 1e-4."""
+    if dtype == torch.float32:
+        return 1e-4, 1e-4, 1e-4
+    return 1e-2, 1e-2, 1e-3
+
+
+def assert_close(name, got, ref, atol, rtol):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values ({np.count_nonzero(~np.isfinite(got))})"
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    if bad.any():
+        idx = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref))), err.shape)
+        raise AssertionError(
+            f"{name}: {int(bad.sum())} of {bad.size} elements outside |d| <= {atol} + {rtol}|ref|;"
+            f" worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}; max abs err {err.max():.3e}")
