@@ -1,0 +1,197 @@
+/*
+ * verify_attn.h -- C ABI of the GB300 (sm_103a) verify-attention library.
+ *
+ * The operation: EAGLE target verification at speculative topk = 1. Each
+ * sequence b has a committed KV prefix of P_b tokens and D_b draft tokens whose
+ * K/V were already written to the same paged cache at logical positions
+ * P_b .. P_b + D_b - 1. Draft row i (query position p = P_b + i) attends,
+ * causally, to keys 0 .. p -- the prefix plus drafts 0 .. i -- optionally cut
+ * by a sliding window to keys p - window .. p.
+ *   Source: "Split-KV flash-decode attention for EAGLE target-verify (Triton
+ *   backend)", Motivation and Modifications: at topk = 1 the draft tree is a
+ *   chain, verification is pure causal attention, the prefix is split across
+ *   parallel programs that each emit a partial output and log-sum-exp, and a
+ *   fused combine merges them with the causal draft x draft block.
+ *   "Support Page Size > 1 (when top k = 1) for FA3 Spec Decode": the tokens of
+ *   a sequence are consecutive in its page table, so page_size > 1 works.
+ *   "Enable EAGLE speculative decoding ... with aiter's unified attention",
+ *   review of the target-verify call: pools viewed [pages, page_size, kv_heads,
+ *   head_dim], output viewed with v_head_dim, window passed as (window, -1).
+ *
+ * Ownership: the caller allocates every buffer (device memory unless stated).
+ * The library allocates nothing, never synchronises inside verify_attn_paged,
+ * and only enqueues work on the caller's stream. A plan and a workspace may be
+ * reused for any number of calls with bs <= plan.max_bs; calls that share one
+ * workspace must be ordered on one stream (they overwrite its contents).
+ *
+ * Streams are passed as `void *` holding a cudaStream_t (NULL = legacy default
+ * stream), so that this header needs no CUDA include.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum va_status {
+    VA_OK = 0,
+    VA_INVALID_ARG = 1,          /* null pointer, negative size, Hq % Hkv != 0, ... */
+    VA_UNSUPPORTED = 2,          /* head dims / row counts outside the compiled set (decided on
+                                    the host from the plan alone, without reading tensors) */
+    VA_WORKSPACE_TOO_SMALL = 3,  /* bs > plan.max_bs, or a plan that does not match the call */
+    VA_CUDA_ERROR = 4,           /* a kernel launch or a CUDA runtime call failed */
+    VA_DEVICE_RANGE_ERROR = 5    /* verify_attn_check only: a device-side check failed */
+};
+
+/* Element type of q, k_cache, v_cache and out. Arithmetic is fp32 throughout. */
+enum va_dtype { VA_FP32 = 0, VA_BF16 = 1, VA_FP16 = 2 };
+
+/* Which prefix kernel a plan selects. */
+enum va_path {
+    VA_PATH_F32 = 1,     /* fp32 inputs: CUDA-core kernel */
+    VA_PATH_MMA = 2,     /* bf16 / fp16 GQA: warp-level tensor-core tiles */
+    VA_PATH_MLA = 3      /* absorbed MLA (one latent kv-head, V aliases K): tcgen05 + TMEM */
+};
+
+/* Bits of the device error word that verify_attn_check reports. A sequence
+ * that fails a check produces NaN rows; other sequences are unaffected. */
+enum va_device_error {
+    VA_ERR_BAD_PAGE = 1,        /* a page id outside [0, num_pages) was met and read as zeros */
+    VA_ERR_SHORT_TABLE = 2,     /* kv_indptr gives fewer pages than ceil((P_b + D_b) / page_size) */
+    VA_ERR_BAD_DRAFT = 4,       /* num_draft[b] < 0 or > plan max_draft */
+    VA_ERR_BAD_LENGTH = 8       /* seq_lens[b] < 0 or P_b + D_b > plan max_kv_len */
+};
+
+/*
+ * Static description of the calls a plan serves.
+ *   max_bs        largest batch any call passes
+ *   max_draft     largest num_draft[b] (1 .. 64)
+ *   num_q_heads   Hq;  num_kv_heads: Hkv, Hq % Hkv == 0 (GQA: q-head h reads
+ *                 kv-head h / (Hq / Hkv))
+ *   qk_dim, v_dim head dims of Q/K and of V / out (may differ)
+ *   page_size     tokens per page (>= 1)
+ *   dtype         enum va_dtype
+ *   v_aliases_k   1: V is the first v_dim entries of each K row (absorbed MLA;
+ *                 v_cache is ignored), 0: separate V pool
+ *   num_ctas      0: automatic; > 0 forces the number of persistent CTAs the
+ *                 prefix kernel splits the KV stream over (tests use it to
+ *                 vary the split-KV partition)
+ *   num_sms       0: query the current device; > 0: use this SM count
+ *   max_kv_len    largest P_b + D_b
+ *   num_pages     pages in the K/V pools; page ids are checked against it
+ */
+typedef struct va_problem {
+    int32_t max_bs;
+    int32_t max_draft;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t qk_dim;
+    int32_t v_dim;
+    int32_t page_size;
+    int32_t dtype;
+    int32_t v_aliases_k;
+    int32_t num_ctas;
+    int32_t num_sms;
+    int32_t reserved0;
+    int64_t max_kv_len;
+    int64_t num_pages;
+} va_problem;
+
+/* Filled by verify_attn_plan. Callers read workspace_bytes; the rest is the
+ * plan's own bookkeeping and must be passed back unchanged. */
+typedef struct va_plan {
+    va_problem problem;
+    int32_t path;             /* enum va_path */
+    int32_t rows_cap;         /* (Hq / Hkv) * max_draft: query rows per kv-head and sequence */
+    int32_t num_ctas;         /* persistent CTAs of the prefix kernel */
+    int32_t num_slots;        /* partial (output, lse) slots per query row */
+    int32_t tile_tokens;      /* KV tokens per prefix tile */
+    int32_t variant;          /* kernel variant within the path */
+    uint64_t workspace_bytes; /* device bytes the caller must provide */
+    uint64_t off_seq;         /* byte offsets inside the workspace */
+    uint64_t off_part_lse;
+    uint64_t off_part_o;
+    uint64_t reserved[4];
+} va_plan;
+
+/*
+ * Plans a family of calls: selects the kernels, the prefix partition and the
+ * workspace size. Host only; it touches the device only when
+ * problem->num_sms == 0 (to read the SM count of the current device).
+ * The workspace size depends on max_bs, never on the per-call batch, so one
+ * workspace at a fixed address serves every call (CUDA-graph friendly); this
+ * follows the split-KV page's review fix of sizing scratch by a stable max_bs.
+ * Returns VA_OK, VA_INVALID_ARG or VA_UNSUPPORTED.
+ */
+int verify_attn_plan(const va_problem *problem, va_plan *plan);
+
+/*
+ * Verify attention for bs sequences (0 <= bs <= plan->problem.max_bs; bs == 0
+ * returns VA_OK and does nothing).
+ *
+ *   q           [sum_b D_b, Hq, qk_dim]  rows grouped by sequence, drafts in order
+ *   k_cache     [num_pages, page_size, Hkv, qk_dim]
+ *   v_cache     [num_pages, page_size, Hkv, v_dim]  (ignored when v_aliases_k)
+ *   page_table  int32, CSR over pages: sequence b's logical page k is
+ *               page_table[kv_indptr[b] + k]; logical token j lives at row
+ *               j % page_size of page page_table[kv_indptr[b] + j / page_size]
+ *   kv_indptr   int32 [bs + 1]; needs kv_indptr[b+1] - kv_indptr[b] >=
+ *               ceil((P_b + D_b) / page_size)
+ *   seq_lens    int32 [bs], P_b: the committed prefix length (drafts excluded)
+ *   num_draft   int32 [bs], D_b: draft tokens of sequence b (0 .. max_draft)
+ *   page_size   must equal plan->problem.page_size
+ *   scale       softmax scale applied to q . k
+ *   window      < 0: no window; >= 0: row at position p sees keys p-window .. p
+ *   out         [sum_b D_b, Hq, v_dim], dtype of the plan (v_dim, not qk_dim)
+ *   lse         fp32 [sum_b D_b, Hq], natural log of sum_j exp(scale q.k_j)
+ *   workspace   plan->workspace_bytes of device memory, 256-byte aligned; its
+ *               contents need no initialisation
+ *   stream      cudaStream_t
+ *
+ * Pointer arguments other than workspace must be 16-byte aligned. Device-side
+ * range checks (page ids, table lengths, draft counts) never trap: they set
+ * bits of the workspace's error word, which verify_attn_check reads.
+ * Returns VA_OK, VA_INVALID_ARG, VA_WORKSPACE_TOO_SMALL or VA_CUDA_ERROR.
+ */
+int verify_attn_paged(const va_plan *plan, int bs, const void *q, const void *k_cache,
+                      const void *v_cache, const int32_t *page_table, const int32_t *kv_indptr,
+                      const int32_t *seq_lens, const int32_t *num_draft, int page_size,
+                      float scale, int window, void *out, float *lse, void *workspace,
+                      void *stream);
+
+/*
+ * verify_attn_paged, plus four CUDA events (cudaEvent_t, created by the caller)
+ * recorded on the stream: before the work-list kernel, before the prefix
+ * kernel, before the combine kernel, and after it. For profiling only.
+ */
+int verify_attn_paged_profiled(const va_plan *plan, int bs, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *page_table,
+                               const int32_t *kv_indptr, const int32_t *seq_lens,
+                               const int32_t *num_draft, int page_size, float scale, int window,
+                               void *out, float *lse, void *workspace, void *stream,
+                               void *const events[4]);
+
+/* Text for a status code (static storage). */
+const char *verify_attn_status_string(int status);
+
+/*
+ * Synchronises the stream, reads the error word that the last call on this
+ * workspace left, and stores it in *error_bits (if not NULL). Returns VA_OK,
+ * VA_DEVICE_RANGE_ERROR when any bit is set, or VA_CUDA_ERROR.
+ */
+int verify_attn_check(const va_plan *plan, const void *workspace, void *stream,
+                      int32_t *error_bits);
+
+/* Number of kernel launches one verify_attn_paged call makes for this plan. */
+int verify_attn_launches_per_call(const va_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

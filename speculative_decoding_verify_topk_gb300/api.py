@@ -1,0 +1,73 @@
+"""VerifyAttention: one plan plus a workspace allocated once at a fixed address.
+
+The workspace is sized by max_bs, not by the per-call batch, so the same
+buffers serve every call and a call can be captured in a CUDA graph (the
+review of "Split-KV flash-decode attention for EAGLE target-verify (Triton
+backend)" asked for exactly this: scratch sized by a stable max_bs instead of
+one buffer per batch size).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding
+
+_DTYPES = {torch.float32: binding.VA_FP32, torch.bfloat16: binding.VA_BF16,
+           torch.float16: binding.VA_FP16}
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    try:
+        return _DTYPES[dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {dtype}") from None
+
+
+class VerifyAttention:
+    def __init__(self, *, max_bs: int, max_draft: int, num_q_heads: int, num_kv_heads: int,
+                 qk_dim: int, v_dim: int, page_size: int, dtype: torch.dtype, max_kv_len: int,
+                 num_pages: int, v_aliases_k: bool = False, num_ctas: int = 0,
+                 device: torch.device | str = "cuda"):
+        self.device = torch.device(device)
+        self.dtype = dtype
+        num_sms = 0
+        if self.device.type == "cuda":
+            num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.plan = binding.verify_attn_plan(
+            max_bs=max_bs, max_draft=max_draft, num_q_heads=num_q_heads,
+            num_kv_heads=num_kv_heads, qk_dim=qk_dim, v_dim=v_dim, page_size=page_size,
+            dtype=dtype_code(dtype), max_kv_len=max_kv_len, num_pages=num_pages,
+            v_aliases_k=v_aliases_k, num_ctas=num_ctas, num_sms=num_sms)
+        self.workspace = torch.empty(int(self.plan.workspace_bytes), dtype=torch.uint8,
+                                     device=self.device)
+        self.num_q_heads, self.v_dim = num_q_heads, v_dim
+
+    @property
+    def launches_per_call(self) -> int:
+        return binding.verify_attn_launches_per_call(self.plan)
+
+    def __call__(self, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft, *,
+                 page_size: int, scale: float, window: int = -1, out=None, lse=None,
+                 stream=None, events=None):
+        """Runs verify attention; returns (out [sum D_b, Hq, v_dim], lse [sum D_b, Hq])."""
+        total_q = q.shape[0]
+        if out is None:
+            out = torch.empty(total_q, self.num_q_heads, self.v_dim, dtype=self.dtype,
+                              device=q.device)
+        if lse is None:
+            lse = torch.empty(total_q, self.num_q_heads, dtype=torch.float32, device=q.device)
+        for name, t in (("q", q), ("k_cache", k_cache), ("out", out)):
+            if t.dtype != self.dtype or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {self.dtype} tensor")
+        for name, t in (("page_table", page_table), ("kv_indptr", kv_indptr),
+                        ("seq_lens", seq_lens), ("num_draft", num_draft)):
+            if t.dtype != torch.int32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 tensor")
+        binding.verify_attn_paged(self.plan, seq_lens.shape[0], q, k_cache, v_cache, page_table,
+                                  kv_indptr, seq_lens, num_draft, page_size, scale, window, out,
+                                  lse, self.workspace, stream=stream, events=events)
+        return out, lse
+
+    def check(self, stream=None) -> int:
+        """Device error bits left by the last call (synchronises the stream)."""
+        return binding.verify_attn_check(self.plan, self.workspace, stream=stream)

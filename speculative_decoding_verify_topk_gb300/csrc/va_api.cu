@@ -1,0 +1,246 @@
+// Host side of the C ABI declared in include/verify_attn.h: planning,
+// argument validation and the three launches of one verify call
+// (work list -> split-KV prefix -> fused combine), all on the caller's stream.
+//
+// The prior art gates its split-KV kernel with a static can_handle() that reads
+// no tensor values and otherwise falls back to a serial kernel ("Split-KV
+// flash-decode attention for EAGLE target-verify (Triton backend)",
+// Modifications). Here the same static decision is made once, in
+// verify_attn_plan, and an unsupported shape is an error (VA_UNSUPPORTED):
+// there is no fallback path.
+#include <cstdint>
+#include <cstring>
+
+#include "va_common.cuh"
+
+namespace va {
+cudaError_t launch_prefix_mma_64x64(const Args&, int, int, cudaStream_t);
+cudaError_t launch_prefix_mma_128x128(const Args&, int, int, cudaStream_t);
+cudaError_t launch_prefix_mma_192x128(const Args&, int, int, cudaStream_t);
+cudaError_t launch_prefix_mma_256x256(const Args&, int, int, cudaStream_t);
+size_t combine_smem_bytes(int max_draft, int qk_dim, int v_dim);
+bool mla_available();
+}  // namespace va
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kSmemLimit = 227 * 1024;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool mma_dims_supported(int qk, int v, int mt) {
+    if (qk == 64 && v == 64) return mt <= 4;
+    if (qk == 128 && v == 128) return mt <= 4;
+    if (qk == 192 && v == 128) return mt <= 4;
+    if (qk == 256 && v == 256) return mt <= 2;
+    return false;
+}
+
+bool is_aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+}  // namespace
+
+extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
+    if (!problem || !plan) return VA_INVALID_ARG;
+    const va_problem p = *problem;
+    if (p.max_bs < 1 || p.max_draft < 1 || p.max_draft > va::kMaxDraft || p.num_q_heads < 1 ||
+        p.num_kv_heads < 1 || p.num_q_heads % p.num_kv_heads != 0 || p.qk_dim < 1 ||
+        p.v_dim < 1 || p.page_size < 1 || p.max_kv_len < 1 || p.max_kv_len > INT32_MAX ||
+        p.num_pages < 1 || p.num_ctas < 0 || p.num_sms < 0)
+        return VA_INVALID_ARG;
+    if (p.dtype != VA_FP32 && p.dtype != VA_BF16 && p.dtype != VA_FP16) return VA_INVALID_ARG;
+    if (p.v_aliases_k && p.v_dim > p.qk_dim) return VA_INVALID_ARG;
+    if ((int64_t)p.max_bs * p.num_kv_heads > 65535) return VA_UNSUPPORTED;   // combine grid.y
+    if (p.v_dim % 32 != 0 || p.v_dim > 512) return VA_UNSUPPORTED;          // combine columns
+    if (va::combine_smem_bytes(p.max_draft, p.qk_dim, p.v_dim) > (size_t)kSmemLimit)
+        return VA_UNSUPPORTED;
+
+    va_plan out;
+    std::memset(&out, 0, sizeof out);
+    out.problem = p;
+    const int group = p.num_q_heads / p.num_kv_heads;
+    if ((int64_t)group * p.max_draft > 4096) return VA_UNSUPPORTED;
+    out.rows_cap = group * p.max_draft;
+    out.tile_tokens = va::kTile;
+
+    int ctas_per_sm = 1;
+    if (p.dtype == VA_FP32) {
+        if (p.qk_dim % 4 != 0) return VA_UNSUPPORTED;
+        const size_t smem = va::prefix_f32_smem_bytes(p.qk_dim, p.v_dim, out.rows_cap);
+        if (smem > (size_t)kSmemLimit) return VA_UNSUPPORTED;
+        out.path = VA_PATH_F32;
+        ctas_per_sm = smem <= 100 * 1024 ? 2 : 1;
+    } else if (p.v_aliases_k && p.num_kv_heads == 1 && p.qk_dim == 576 && p.v_dim == 512 &&
+               p.dtype == VA_BF16 && va::mla_available() && out.rows_cap <= 1024) {
+        out.path = VA_PATH_MLA;
+        ctas_per_sm = 1;
+    } else {
+        const int mt = (out.rows_cap + 15) / 16;
+        if (!mma_dims_supported(p.qk_dim, p.v_dim, mt)) return VA_UNSUPPORTED;
+        out.path = VA_PATH_MMA;
+        out.variant = mt;
+        ctas_per_sm = mt >= 4 ? 1 : 2;
+    }
+
+    int sms = p.num_sms;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return VA_CUDA_ERROR;
+        }
+    }
+    out.num_ctas = p.num_ctas > 0 ? p.num_ctas : sms * ctas_per_sm;
+    const int64_t slots = (int64_t)p.num_kv_heads * p.max_bs + out.num_ctas;
+    if (slots > INT32_MAX) return VA_UNSUPPORTED;
+    out.num_slots = (int)slots;
+
+    size_t off = align_up(va::kHeaderBytes);
+    out.off_seq = off;
+    off = align_up(off + sizeof(va::SeqInfo) * (size_t)p.max_bs);
+    out.off_part_lse = off;
+    off = align_up(off + sizeof(float) * (size_t)slots * out.rows_cap);
+    out.off_part_o = off;
+    off = align_up(off + sizeof(float) * (size_t)slots * out.rows_cap * p.v_dim);
+    out.workspace_bytes = off;
+    *plan = out;
+    return VA_OK;
+}
+
+namespace {
+
+int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
+        const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
+        const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
+        void* workspace, void* stream, void* const* events) {
+    if (!plan) return VA_INVALID_ARG;
+    const va_problem& p = plan->problem;
+    if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_MLA || plan->num_ctas < 1 ||
+        plan->rows_cap < 1 || plan->workspace_bytes == 0)
+        return VA_INVALID_ARG;
+    if (bs < 0) return VA_INVALID_ARG;
+    if (bs > p.max_bs) return VA_WORKSPACE_TOO_SMALL;
+    if (page_size != p.page_size) return VA_INVALID_ARG;
+    if (!(scale == scale)) return VA_INVALID_ARG;
+    if (bs == 0) return VA_OK;
+    if (!q || !k_cache || (!v_cache && !p.v_aliases_k) || !page_table || !kv_indptr ||
+        !seq_lens || !num_draft || !out || !lse || !workspace)
+        return VA_INVALID_ARG;
+    if (!is_aligned(q, 16) || !is_aligned(k_cache, 16) || (!p.v_aliases_k && !is_aligned(v_cache, 16)) ||
+        !is_aligned(out, 16) || !is_aligned(lse, 4) || !is_aligned(workspace, kAlign) ||
+        !is_aligned(page_table, 4) || !is_aligned(kv_indptr, 4) || !is_aligned(seq_lens, 4) ||
+        !is_aligned(num_draft, 4))
+        return VA_INVALID_ARG;
+
+    va::Args a;
+    std::memset(&a, 0, sizeof a);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = p.v_aliases_k ? k_cache : v_cache;
+    a.page_table = page_table;
+    a.kv_indptr = kv_indptr;
+    a.seq_lens = seq_lens;
+    a.num_draft = num_draft;
+    a.out = out;
+    a.lse = lse;
+    a.header = reinterpret_cast<int32_t*>(ws);
+    a.seq = reinterpret_cast<va::SeqInfo*>(ws + plan->off_seq);
+    a.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
+    a.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
+    a.num_pages = p.num_pages;
+    a.max_kv_len = p.max_kv_len;
+    a.k_row_stride = p.qk_dim;
+    a.v_row_stride = p.v_aliases_k ? p.qk_dim : p.v_dim;
+    a.bs = bs;
+    a.hq = p.num_q_heads;
+    a.hkv = p.num_kv_heads;
+    a.group = p.num_q_heads / p.num_kv_heads;
+    a.qk_dim = p.qk_dim;
+    a.v_dim = p.v_dim;
+    a.page_size = p.page_size;
+    a.window = window < 0 ? -1 : window;
+    a.rows_cap = plan->rows_cap;
+    a.max_draft = p.max_draft;
+    a.num_ctas = plan->num_ctas;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto rec = [&](int i) {
+        if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+    };
+    cudaError_t e;
+    rec(0);
+    e = va::launch_worklist(a, s);
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    rec(1);
+    switch (plan->path) {
+    case VA_PATH_F32: e = va::launch_prefix_f32(a, s); break;
+    case VA_PATH_MLA: e = va::launch_prefix_mla(a, s); break;
+    default:
+        if (p.qk_dim == 64) e = va::launch_prefix_mma_64x64(a, p.dtype, plan->variant, s);
+        else if (p.qk_dim == 128) e = va::launch_prefix_mma_128x128(a, p.dtype, plan->variant, s);
+        else if (p.qk_dim == 192) e = va::launch_prefix_mma_192x128(a, p.dtype, plan->variant, s);
+        else e = va::launch_prefix_mma_256x256(a, p.dtype, plan->variant, s);
+    }
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    rec(2);
+    e = va::launch_combine(a, p.dtype, s);
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    rec(3);
+    return VA_OK;
+}
+
+}  // namespace
+
+extern "C" int verify_attn_paged(const va_plan* plan, int bs, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* page_table,
+                                 const int32_t* kv_indptr, const int32_t* seq_lens,
+                                 const int32_t* num_draft, int page_size, float scale, int window,
+                                 void* out, float* lse, void* workspace, void* stream) {
+    return run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
+               page_size, scale, window, out, lse, workspace, stream, nullptr);
+}
+
+extern "C" int verify_attn_paged_profiled(const va_plan* plan, int bs, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* page_table, const int32_t* kv_indptr,
+                                          const int32_t* seq_lens, const int32_t* num_draft,
+                                          int page_size, float scale, int window, void* out,
+                                          float* lse, void* workspace, void* stream,
+                                          void* const events[4]) {
+    if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return VA_INVALID_ARG;
+    return run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
+               page_size, scale, window, out, lse, workspace, stream, events);
+}
+
+extern "C" const char* verify_attn_status_string(int status) {
+    switch (status) {
+    case VA_OK: return "ok";
+    case VA_INVALID_ARG: return "invalid argument";
+    case VA_UNSUPPORTED: return "unsupported shape (no compiled kernel for these head dims / rows)";
+    case VA_WORKSPACE_TOO_SMALL: return "batch larger than the plan's max_bs";
+    case VA_CUDA_ERROR: return "CUDA error";
+    case VA_DEVICE_RANGE_ERROR: return "a device-side range check failed";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int verify_attn_check(const va_plan* plan, const void* workspace, void* stream,
+                                 int32_t* error_bits) {
+    if (!plan || !workspace) return VA_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VA_CUDA_ERROR;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return VA_CUDA_ERROR;
+    if (error_bits) *error_bits = word;
+    return word ? VA_DEVICE_RANGE_ERROR : VA_OK;
+}
+
+extern "C" int verify_attn_launches_per_call(const va_plan* plan) {
+    return plan ? 3 : 0;
+}

@@ -1,0 +1,108 @@
+// Work-list kernel: per-sequence facts for the prefix and combine kernels.
+//
+// One CTA of 1024 threads. For every sequence it checks the lengths and the
+// page-table capacity, derives the prefix range any row can see (the window's
+// lowest bound belongs to row 0), counts the 64-token prefix tiles, and takes
+// two exclusive prefix sums: query rows (qoff) and tiles (tile_off). The grid
+// of the later kernels depends only on host-known sizes; everything that
+// depends on tensor values is computed here, on the device, so a call can be
+// captured in a CUDA graph and replayed with new lengths (the split-KV page's
+// review asks for fixed-address scratch for the same reason).
+#include "va_common.cuh"
+
+namespace va {
+namespace {
+
+constexpr int kThreads = 1024;
+
+// Block-wide exclusive scan of one value per thread; returns the block total.
+__device__ int block_exclusive_scan(int v, int* excl, int* warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        warp_sums[lane] = wi - w;   // exclusive warp offsets
+        if (lane == 31) warp_sums[32] = wi;
+    }
+    __syncthreads();
+    *excl = incl - v + warp_sums[warp];
+    int total = warp_sums[32];
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
+    __shared__ int warp_sums[33];
+    if (threadIdx.x == 0) a.header[kHdrError] = 0;
+    __syncthreads();
+
+    int q_carry = 0, tile_carry = 0, err = 0;
+    for (int base = 0; base < a.bs; base += kThreads) {
+        const int b = base + threadIdx.x;
+        int qrows = 0, tiles = 0;
+        SeqInfo si = {};
+        if (b < a.bs) {
+            const int p = __ldg(a.seq_lens + b);
+            const int d = __ldg(a.num_draft + b);
+            int bad = 0;
+            if (d < 0 || d > a.max_draft) bad |= VA_ERR_BAD_DRAFT;
+            if (p < 0 || (int64_t)p + (d > 0 ? d : 0) > a.max_kv_len) bad |= VA_ERR_BAD_LENGTH;
+            if (!bad) {
+                const int64_t need = ((int64_t)p + d + a.page_size - 1) / a.page_size;
+                const int64_t have = (int64_t)__ldg(a.kv_indptr + b + 1) - __ldg(a.kv_indptr + b);
+                if (have < need) bad |= VA_ERR_SHORT_TABLE;
+            }
+            err |= bad;
+            si.prefix = p;
+            si.bad = bad;
+            // A failed sequence keeps its query rows (so later sequences keep
+            // their place and the combine can mark its rows NaN) but reads no KV.
+            qrows = d > 0 ? d : 0;
+            si.draft = qrows < a.max_draft ? qrows : a.max_draft;
+            if (!bad && qrows > 0) {
+                const int lo = (a.window >= 0 && p - a.window > 0) ? p - a.window : 0;
+                si.lo = lo;
+                si.a0 = lo & ~(kTile - 1);
+                tiles = p > lo ? (p - si.a0 + kTile - 1) / kTile : 0;
+            }
+            si.tiles = tiles;
+        }
+        int q_excl, t_excl;
+        const int q_tot = block_exclusive_scan(qrows, &q_excl, warp_sums);
+        const int t_tot = block_exclusive_scan(tiles, &t_excl, warp_sums);
+        if (b < a.bs) {
+            si.qoff = q_carry + q_excl;
+            si.tile_off = tile_carry + t_excl;
+            a.seq[b] = si;
+        }
+        q_carry += q_tot;
+        tile_carry += t_tot;
+    }
+    if (err) set_error(a, err);
+    if (threadIdx.x == 0) {
+        a.header[kHdrTotalTiles] = tile_carry;
+        a.header[kHdrBs] = a.bs;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_worklist(const Args& a, cudaStream_t s) {
+    worklist_kernel<<<1, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace va

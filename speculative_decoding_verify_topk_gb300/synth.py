@@ -251,3 +251,27 @@ def kv_token_bytes(wl: Workload) -> int:
     """Bytes of K (+ V unless aliased) that one KV token carries across all kv-heads."""
     e = torch.finfo(wl.dtype).bits // 8
     return wl.num_kv_heads * (wl.qk_dim + (0 if wl.v_aliases_k else wl.v_dim)) * e
+
+
+def subset(pb: Paged, seqs) -> Paged:
+    """The sequences `seqs` of a batch as a batch of their own, on the host,
+    with a compact pool holding only their pages (page ids renumbered in
+    order). Row results of the subset equal those rows of the full batch; this
+    is how a host-side checker reads a slice of a multi-GB device pool."""
+    seqs = [int(s) for s in seqs]
+    indptr = pb.kv_indptr.cpu().to(torch.int64)
+    table = pb.page_table.cpu().to(torch.int64)
+    ndraft = pb.num_draft.cpu()
+    qoff = torch.zeros(len(ndraft) + 1, dtype=torch.int64)
+    qoff[1:] = torch.cumsum(ndraft.to(torch.int64), 0)
+    pages = torch.cat([table[int(indptr[b]):int(indptr[b + 1])] for b in seqs])
+    new_indptr = torch.zeros(len(seqs) + 1, dtype=torch.int32)
+    new_indptr[1:] = torch.cumsum(torch.tensor([int(indptr[b + 1] - indptr[b]) for b in seqs]), 0)
+    dev_pages = pages.to(pb.k_cache.device)
+    k_cache = pb.k_cache.index_select(0, dev_pages).cpu()
+    v_cache = k_cache if pb.v_cache is pb.k_cache else pb.v_cache.index_select(0, dev_pages).cpu()
+    q = torch.cat([pb.q[int(qoff[b]):int(qoff[b + 1])] for b in seqs]).cpu()
+    sel = torch.tensor(seqs, dtype=torch.int64)
+    wl = pb.wl.replace(bs=len(seqs))
+    return Paged(wl, q, k_cache, v_cache, torch.arange(len(pages), dtype=torch.int32), new_indptr,
+                 pb.seq_lens.cpu()[sel].contiguous(), ndraft[sel].contiguous(), pb.page_size)

@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/verify_attn.h declares, its structs have the header's layout, and
+planning / host-side validation behave as documented (no kernel launches)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import speculative_decoding_verify_topk_gb300 as va
+from speculative_decoding_verify_topk_gb300 import binding
+from speculative_decoding_verify_topk_gb300 import build as va_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    va_build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(HEADER_DIR)):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(verify_attn_\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "verify_attn_plan" in names and "verify_attn_paged" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text("""
+#include <stdio.h>
+#include <stddef.h>
+#include "verify_attn.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(va_problem), sizeof(va_plan),
+         offsetof(va_problem, max_kv_len), offsetof(va_plan, path),
+         offsetof(va_plan, workspace_bytes), offsetof(va_plan, reserved));
+  return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    subprocess.run(["cc", "-I", HEADER_DIR, "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(binding.Problem), ctypes.sizeof(binding.Plan),
+            binding.Problem.max_kv_len.offset, binding.Plan.path.offset,
+            binding.Plan.workspace_bytes.offset, binding.Plan.reserved.offset]
+    assert got == want
+
+
+def _plan(**kw):
+    base = dict(max_bs=16, max_draft=4, num_q_heads=32, num_kv_heads=8, qk_dim=128, v_dim=128,
+                page_size=4, dtype=va.VA_BF16, max_kv_len=8200, num_pages=1 << 19, num_sms=152)
+    base.update(kw)
+    return va.verify_attn_plan(**base)
+
+
+def test_plan_selects_paths(lib):
+    p = _plan()
+    assert p.path == va.VA_PATH_MMA and p.variant == 1 and p.rows_cap == 16
+    assert p.num_ctas == 152 * 2
+    assert p.num_slots == 8 * 16 + p.num_ctas
+    assert p.workspace_bytes % 256 == 0 and p.workspace_bytes >= (
+        p.off_part_o + 4 * p.num_slots * p.rows_cap * 128)
+    assert _plan(dtype=va.VA_FP32, qk_dim=64, v_dim=64, num_q_heads=4, num_kv_heads=2).path == va.VA_PATH_F32
+    mixed = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128)
+    assert mixed.path == va.VA_PATH_MMA and mixed.variant == 3  # 40 rows -> 3 m16 tiles
+    assert _plan(num_ctas=7).num_ctas == 7
+
+
+def test_workspace_depends_on_max_bs_only(lib):
+    a, b = _plan(max_kv_len=1 << 20), _plan(max_kv_len=4096)
+    assert a.workspace_bytes == b.workspace_bytes
+    assert _plan(max_bs=64).workspace_bytes > a.workspace_bytes
+
+
+@pytest.mark.parametrize("kw", [dict(num_q_heads=30, num_kv_heads=8), dict(max_draft=0),
+                                dict(max_bs=0), dict(page_size=0), dict(dtype=7),
+                                dict(v_aliases_k=True, qk_dim=64, v_dim=128),
+                                dict(max_draft=65), dict(num_pages=0)])
+def test_plan_rejects_invalid(lib, kw):
+    with pytest.raises(va.VerifyAttnError) as e:
+        _plan(**kw)
+    assert e.value.status == binding.VA_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(qk_dim=96, v_dim=96), dict(num_q_heads=128, num_kv_heads=8,
+                                                                max_draft=8)])
+def test_plan_reports_unsupported(lib, kw):
+    with pytest.raises(va.VerifyAttnError) as e:
+        _plan(**kw)
+    assert e.value.status == binding.VA_UNSUPPORTED
+
+
+def test_call_validation_without_launch(lib):
+    """Host-side checks that return before any CUDA call."""
+    p = _plan()
+    fake = ctypes.c_void_p(256)  # never dereferenced: each call below returns first
+    call = lambda bs, ps=4, **kw: lib.verify_attn_paged(
+        ctypes.byref(p), bs, *([kw.get("q", fake)] + [fake] * 6), ps, 0.1, -1, fake, fake,
+        kw.get("ws", fake), None)
+    assert call(0) == binding.VA_OK                       # empty batch: nothing to do
+    assert call(17) == binding.VA_WORKSPACE_TOO_SMALL     # bs > max_bs
+    assert call(-1) == binding.VA_INVALID_ARG
+    assert call(4, ps=8) == binding.VA_INVALID_ARG        # page size differs from the plan
+    assert call(4, q=None) == binding.VA_INVALID_ARG      # null pointer
+    assert call(4, q=ctypes.c_void_p(264)) == binding.VA_INVALID_ARG  # q not 16-byte aligned
+    assert call(4, ws=ctypes.c_void_p(272)) == binding.VA_INVALID_ARG  # workspace not 256-aligned
+    assert lib.verify_attn_launches_per_call(ctypes.byref(p)) == 3
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert va.status_string(s) not in ("", "unknown status")
+    assert va.status_string(99) == "unknown status"
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(ImportError, match="no fallback"):
+        # a fresh loader pointed at a missing file must raise, not fall back
+        saved = binding._lib
+        try:
+            binding._lib = None
+            binding.load_library(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = saved
