@@ -64,6 +64,9 @@ def parse():
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="pool of 1.25x the pages the batch uses instead of the workload's own "
+                         "pool size (same kernels and results; for profiler captures)")
     return ap.parse_args()
 
 
@@ -315,6 +318,8 @@ def ours_arm(args):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     wl = synth.WORKLOADS[args.workload]
+    if args.compact_pool:
+        wl = wl.replace(pool_tokens=None)
     window = wl.window_for_call(0)
     pb = synth.make_batch(wl, device=dev, seed=wl.seed + 1000 * rank)
     lens = pb.seq_lens.long() + pb.num_draft.long()

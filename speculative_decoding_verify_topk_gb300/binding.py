@@ -129,7 +129,12 @@ def verify_attn_paged(plan: Plan, bs: int, q, k_cache, v_cache, page_table, kv_i
     if events is None:
         rc = lib.verify_attn_paged(*args)
     else:
-        ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+        handles = []
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+                e.record()
+            handles.append(e.cuda_event)
+        ev = (ctypes.c_void_p * 4)(*handles)
         rc = lib.verify_attn_paged_profiled(*args, ev)
     if rc != VA_OK:
         raise VerifyAttnError(rc, "verify_attn_paged")

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
 
         // prefix partials
         for (int c = c_first; c <= c_last; ++c) {
+            // a CTA whose stream range is empty (more CTAs than tiles) wrote nothing
+            if (cta_start(c + 1, work, a.num_ctas) == cta_start(c, work, a.num_ctas)) continue;
             const int64_t pr = (int64_t)(g * a.bs + b + c) * a.rows_cap + r;
             const float lc = a.part_lse[pr];
             if (lc == -INFINITY) continue;
