@@ -190,6 +190,36 @@ int verify_attn_check(const va_plan *plan, const void *workspace, void *stream,
 /* Number of kernel launches one verify_attn_paged call makes for this plan. */
 int verify_attn_launches_per_call(const va_plan *plan);
 
+/*
+ * verify_attn_paged for callers that cannot allocate device memory. The pages
+ * this library follows have no counterpart of it; it exists for programs such
+ * as plugins inside a host application that owns all device memory through its
+ * own pool and offers them no allocator, or latency-critical code where
+ * cudaMalloc (which can synchronise the device) is not allowed.
+ *
+ * Arguments are those of verify_attn_paged without the workspace: the scratch
+ * is a static device array of VA_STATIC_WORKSPACE_BYTES inside this library,
+ * which every GPU that loads the library holds until the process exits. The
+ * caller still provides all inputs and outputs. No call allocates or frees.
+ *
+ * - Plans whose workspace_bytes exceed VA_STATIC_WORKSPACE_BYTES are rejected
+ *   with VA_WORKSPACE_TOO_SMALL before anything is launched.
+ * - The first call on a device, made with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that first
+ *   call before any stream capture.
+ * - All calls on a device share the one array, and it keeps whatever the last
+ *   call left; the kernels need none of it to start cleared. Calls whose
+ *   executions overlap on the GPU (different streams, or different host
+ *   threads) race on the array: order them on one stream.
+ * Returns the codes of verify_attn_paged.
+ */
+#define VA_STATIC_WORKSPACE_BYTES (32u << 20)
+int verify_attn_paged_static(const va_plan *plan, int bs, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *page_table,
+                             const int32_t *kv_indptr, const int32_t *seq_lens,
+                             const int32_t *num_draft, int page_size, float scale, int window,
+                             void *out, float *lse, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,8 @@ VA_PATH_F32, VA_PATH_MMA, VA_PATH_MLA = 1, 2, 3
 VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH = 1, 2, 4, 8
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
-           "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call")
+           "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
+           "verify_attn_paged_static")
 
 
 class Problem(ctypes.Structure):

@@ -109,7 +109,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     return VA_OK;
 }
 
-namespace {
+namespace va {
 
 int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
@@ -194,15 +194,15 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     return VA_OK;
 }
 
-}  // namespace
+}  // namespace va
 
 extern "C" int verify_attn_paged(const va_plan* plan, int bs, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* page_table,
                                  const int32_t* kv_indptr, const int32_t* seq_lens,
                                  const int32_t* num_draft, int page_size, float scale, int window,
                                  void* out, float* lse, void* workspace, void* stream) {
-    return run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
-               page_size, scale, window, out, lse, workspace, stream, nullptr);
+    return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
+                   page_size, scale, window, out, lse, workspace, stream, nullptr);
 }
 
 extern "C" int verify_attn_paged_profiled(const va_plan* plan, int bs, const void* q,
@@ -213,8 +213,8 @@ extern "C" int verify_attn_paged_profiled(const va_plan* plan, int bs, const voi
                                           float* lse, void* workspace, void* stream,
                                           void* const events[4]) {
     if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return VA_INVALID_ARG;
-    return run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
-               page_size, scale, window, out, lse, workspace, stream, events);
+    return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
+                   page_size, scale, window, out, lse, workspace, stream, events);
 }
 
 extern "C" const char* verify_attn_status_string(int status) {

@@ -74,6 +74,13 @@ struct Args {
     float scale;
 };
 
+// One verify call on a caller-provided workspace (validation + the three
+// launches); the C entry points are thin wrappers around it.
+int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
+        const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
+        const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
+        void* workspace, void* stream, void* const* events);
+
 // Host-side launchers (one per translation unit).
 cudaError_t launch_worklist(const Args& a, cudaStream_t s);
 cudaError_t launch_prefix_mma(const Args& a, int dtype, int variant, cudaStream_t s);
