@@ -64,13 +64,15 @@ enum va_device_error {
     VA_ERR_BAD_PAGE = 1,        /* a page id outside [0, num_pages) was met and read as zeros */
     VA_ERR_SHORT_TABLE = 2,     /* kv_indptr gives fewer pages than ceil((P_b + D_b) / page_size) */
     VA_ERR_BAD_DRAFT = 4,       /* num_draft[b] < 0 or > plan max_draft */
-    VA_ERR_BAD_LENGTH = 8       /* seq_lens[b] < 0 or P_b + D_b > plan max_kv_len */
+    VA_ERR_BAD_LENGTH = 8,      /* seq_lens[b] < 0 or P_b + D_b > plan max_kv_len */
+    VA_ERR_TIMEOUT = 16         /* an internal pipeline wait gave up (never expected; the
+                                   kernel stops early instead of hanging) */
 };
 
 /*
  * Static description of the calls a plan serves.
  *   max_bs        largest batch any call passes
- *   max_draft     largest num_draft[b] (1 .. 64)
+ *   max_draft     largest num_draft[b] (1 .. 32)
  *   num_q_heads   Hq;  num_kv_heads: Hkv, Hq % Hkv == 0 (GQA: q-head h reads
  *                 kv-head h / (Hq / Hkv))
  *   qk_dim, v_dim head dims of Q/K and of V / out (may differ)
@@ -111,12 +113,16 @@ typedef struct va_plan {
     int32_t num_ctas;         /* persistent CTAs of the prefix kernel */
     int32_t num_slots;        /* partial (output, lse) slots per query row */
     int32_t tile_tokens;      /* KV tokens per prefix tile */
-    int32_t variant;          /* kernel variant within the path */
+    int32_t variant;          /* kernel variant within the path (m16 row tiles per kv-head) */
     uint64_t workspace_bytes; /* device bytes the caller must provide */
     uint64_t off_seq;         /* byte offsets inside the workspace */
     uint64_t off_part_lse;
     uint64_t off_part_o;
-    uint64_t reserved[4];
+    int32_t heads_per_cta;    /* kv-heads one prefix CTA processes together */
+    int32_t box_tokens;       /* tokens per bulk-tensor copy (gcd(page_size, tile_tokens)) */
+    int32_t stages;           /* shared-memory ring depth of the prefix kernel */
+    int32_t stage_bytes;      /* bytes per ring stage */
+    uint64_t reserved[2];
 } va_plan;
 
 /*

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libverify_attn.so")
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_WORKSPACE_TOO_SMALL, VA_CUDA_ERROR, VA_DEVICE_RANGE_ERROR = range(6)
 VA_FP32, VA_BF16, VA_FP16 = 0, 1, 2
 VA_PATH_F32, VA_PATH_MMA, VA_PATH_MLA = 1, 2, 3
-VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH = 1, 2, 4, 8
+VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
@@ -41,7 +41,9 @@ class Plan(ctypes.Structure):
                 ("tile_tokens", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_uint64), ("off_seq", ctypes.c_uint64),
                 ("off_part_lse", ctypes.c_uint64), ("off_part_o", ctypes.c_uint64),
-                ("reserved", ctypes.c_uint64 * 4)]
+                ("heads_per_cta", ctypes.c_int32), ("box_tokens", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("reserved", ctypes.c_uint64 * 2)]
 
 
 class VerifyAttnError(RuntimeError):

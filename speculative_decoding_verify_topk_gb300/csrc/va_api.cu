@@ -8,18 +8,75 @@
 // Modifications). Here the same static decision is made once, in
 // verify_attn_plan, and an unsupported shape is an error (VA_UNSUPPORTED):
 // there is no fallback path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <cstring>
 
 #include "va_common.cuh"
 
 namespace va {
-cudaError_t launch_prefix_mma_64x64(const Args&, int, int, cudaStream_t);
-cudaError_t launch_prefix_mma_128x128(const Args&, int, int, cudaStream_t);
-cudaError_t launch_prefix_mma_192x128(const Args&, int, int, cudaStream_t);
-cudaError_t launch_prefix_mma_256x256(const Args&, int, int, cudaStream_t);
-size_t combine_smem_bytes(int max_draft, int qk_dim, int v_dim);
+using MmaLaunch = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&,
+                                  int, cudaStream_t);
+cudaError_t launch_prefix_mma_64x64(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
+cudaError_t launch_prefix_mma_128x128(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
+cudaError_t launch_prefix_mma_192x128(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
+cudaError_t launch_prefix_mma_256x256(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
 bool mla_available();
+
+static MmaLaunch mma_launcher(int qk, int v) {
+    if (qk == 64 && v == 64) return launch_prefix_mma_64x64;
+    if (qk == 128 && v == 128) return launch_prefix_mma_128x128;
+    if (qk == 192 && v == 128) return launch_prefix_mma_192x128;
+    if (qk == 256 && v == 256) return launch_prefix_mma_256x256;
+    return nullptr;
+}
+bool prefix_mma_built(int qk, int v) { return mma_launcher(qk, v) != nullptr; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 3-d map {columns, token slot, kv-head} over a paged pool whose (slot, head)
+// rows hold `row_elems` elements; boxes of 64 columns x tb tokens x hg heads,
+// landing in shared memory as [head][token][64] with the 128-byte swizzle.
+static bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, int cols, int row_elems,
+                            int64_t slots, int hkv, int tb, int hg) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)slots, (cuuint64_t)hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)hkv * row_elems * 2, (cuuint64_t)row_elems * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)tb, (cuuint32_t)hg};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == VA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int gcd_int(int x, int y) {
+    while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
+    }
+    return x;
+}
 }  // namespace va
 
 namespace {
@@ -28,14 +85,6 @@ constexpr size_t kAlign = 256;
 constexpr int kSmemLimit = 227 * 1024;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
-
-bool mma_dims_supported(int qk, int v, int mt) {
-    if (qk == 64 && v == 64) return mt <= 4;
-    if (qk == 128 && v == 128) return mt <= 4;
-    if (qk == 192 && v == 128) return mt <= 4;
-    if (qk == 256 && v == 256) return mt <= 2;
-    return false;
-}
 
 bool is_aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
@@ -52,9 +101,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     if (p.dtype != VA_FP32 && p.dtype != VA_BF16 && p.dtype != VA_FP16) return VA_INVALID_ARG;
     if (p.v_aliases_k && p.v_dim > p.qk_dim) return VA_INVALID_ARG;
     if ((int64_t)p.max_bs * p.num_kv_heads > 65535) return VA_UNSUPPORTED;   // combine grid.y
-    if (p.v_dim % 32 != 0 || p.v_dim > 512) return VA_UNSUPPORTED;          // combine columns
-    if (va::combine_smem_bytes(p.max_draft, p.qk_dim, p.v_dim) > (size_t)kSmemLimit)
-        return VA_UNSUPPORTED;
+    if (!va::combine_supported(p.qk_dim, p.v_dim)) return VA_UNSUPPORTED;
 
     va_plan out;
     std::memset(&out, 0, sizeof out);
@@ -62,7 +109,6 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     const int group = p.num_q_heads / p.num_kv_heads;
     if ((int64_t)group * p.max_draft > 4096) return VA_UNSUPPORTED;
     out.rows_cap = group * p.max_draft;
-    out.tile_tokens = va::kTile;
 
     int ctas_per_sm = 1;
     if (p.dtype == VA_FP32) {
@@ -71,17 +117,36 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         if (smem > (size_t)kSmemLimit) return VA_UNSUPPORTED;
         out.path = VA_PATH_F32;
         ctas_per_sm = smem <= 100 * 1024 ? 2 : 1;
+        out.tile_tokens = va::kTile;
     } else if (p.v_aliases_k && p.num_kv_heads == 1 && p.qk_dim == 576 && p.v_dim == 512 &&
                p.dtype == VA_BF16 && va::mla_available() && out.rows_cap <= 1024) {
         out.path = VA_PATH_MLA;
         ctas_per_sm = 1;
     } else {
+        // bf16 / fp16: a CTA takes hg kv-heads (the largest divisor of Hkv with
+        // hg * mt <= 8 consumer warps) over 16-token tiles fed by TMA boxes of
+        // gcd(page_size, 16) tokens
         const int mt = (out.rows_cap + 15) / 16;
-        if (!mma_dims_supported(p.qk_dim, p.v_dim, mt)) return VA_UNSUPPORTED;
+        if (mt > 8 || !va::prefix_mma_built(p.qk_dim, p.v_dim)) return VA_UNSUPPORTED;
+        int hg = 1;
+        for (int d = 1; d <= p.num_kv_heads && d * mt <= 8; ++d)
+            if (p.num_kv_heads % d == 0) hg = d;
+        const int tb = va::gcd_int(p.page_size, 16);
+        const int box_stride = (tb * hg * 128 + 1023) / 1024 * 1024;
+        const int stage = (p.qk_dim / 64 + p.v_dim / 64) * (16 / tb) * box_stride;
+        int stages = (kSmemLimit - 2048) / stage;
+        if (stages > 8) stages = 8;
+        if (stages < 2) return VA_UNSUPPORTED;
         out.path = VA_PATH_MMA;
         out.variant = mt;
-        ctas_per_sm = mt >= 4 ? 1 : 2;
+        out.tile_tokens = 16;
+        out.heads_per_cta = hg;
+        out.box_tokens = tb;
+        out.stages = stages;
+        out.stage_bytes = stage;
+        ctas_per_sm = 1;   // one warp-specialised CTA fills an SM's shared memory
     }
+    if (out.heads_per_cta == 0) out.heads_per_cta = 1;
 
     int sms = p.num_sms;
     if (sms == 0) {
@@ -93,7 +158,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         }
     }
     out.num_ctas = p.num_ctas > 0 ? p.num_ctas : sms * ctas_per_sm;
-    const int64_t slots = (int64_t)p.num_kv_heads * p.max_bs + out.num_ctas;
+    const int64_t slots = (int64_t)p.num_kv_heads * p.max_bs + (int64_t)out.heads_per_cta * out.num_ctas;
     if (slots > INT32_MAX) return VA_UNSUPPORTED;
     out.num_slots = (int)slots;
 
@@ -118,7 +183,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     if (!plan) return VA_INVALID_ARG;
     const va_problem& p = plan->problem;
     if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_MLA || plan->num_ctas < 1 ||
-        plan->rows_cap < 1 || plan->workspace_bytes == 0)
+        plan->rows_cap < 1 || plan->workspace_bytes == 0 || plan->tile_tokens < 1)
         return VA_INVALID_ARG;
     if (bs < 0) return VA_INVALID_ARG;
     if (bs > p.max_bs) return VA_WORKSPACE_TOO_SMALL;
@@ -165,6 +230,9 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.rows_cap = plan->rows_cap;
     a.max_draft = p.max_draft;
     a.num_ctas = plan->num_ctas;
+    a.tile = plan->tile_tokens;
+    a.hg = plan->heads_per_cta;
+    if (a.hg < 1 || p.num_kv_heads % a.hg != 0) return VA_INVALID_ARG;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
 
@@ -180,11 +248,33 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     switch (plan->path) {
     case VA_PATH_F32: e = va::launch_prefix_f32(a, s); break;
     case VA_PATH_MLA: e = va::launch_prefix_mla(a, s); break;
-    default:
-        if (p.qk_dim == 64) e = va::launch_prefix_mma_64x64(a, p.dtype, plan->variant, s);
-        else if (p.qk_dim == 128) e = va::launch_prefix_mma_128x128(a, p.dtype, plan->variant, s);
-        else if (p.qk_dim == 192) e = va::launch_prefix_mma_192x128(a, p.dtype, plan->variant, s);
-        else e = va::launch_prefix_mma_256x256(a, p.dtype, plan->variant, s);
+    default: {
+        va::Geo g;
+        g.hg = plan->heads_per_cta;
+        g.mt = plan->variant;
+        g.nc = g.hg * g.mt;
+        g.tb = plan->box_tokens;
+        g.ppt = plan->tile_tokens / g.tb;
+        g.box_stride = (g.tb * g.hg * 128 + 1023) / 1024 * 1024;
+        g.half_bytes = g.ppt * g.box_stride;
+        g.nhk = p.qk_dim / 64;
+        g.nhv = p.v_dim / 64;
+        g.stage_bytes = plan->stage_bytes;
+        g.stages = plan->stages;
+        g.tx_box = (uint32_t)(g.tb * g.hg * 128);
+        const va::MmaLaunch fn = va::mma_launcher(p.qk_dim, p.v_dim);
+        const int64_t slots = p.num_pages * p.page_size;
+        CUtensorMap kmap, vmap;
+        if (!fn || g.nc < 1 || g.nc > 8 || g.ppt * g.tb != plan->tile_tokens ||
+            g.stage_bytes != (g.nhk + g.nhv) * g.half_bytes)
+            return VA_INVALID_ARG;
+        if (!va::encode_pool_map(&kmap, a.k_cache, p.dtype, p.qk_dim, p.qk_dim, slots,
+                                 p.num_kv_heads, g.tb, g.hg) ||
+            !va::encode_pool_map(&vmap, a.v_cache, p.dtype, p.v_dim, (int)a.v_row_stride, slots,
+                                 p.num_kv_heads, g.tb, g.hg))
+            return VA_CUDA_ERROR;
+        e = fn(kmap, vmap, a, g, p.dtype, s);
+    }
     }
     if (e != cudaSuccess) return VA_CUDA_ERROR;
     rec(2);

@@ -7,14 +7,15 @@
 // draft keys it sees are the cache positions P_b + k for
 // max(0, i - window) <= k <= i (all k <= i without a window). Their scores are
 // exact dot products here; the prefix contributes one (lse_c, o_c) pair per
-// segment that covered (g, b). Every term is merged with a running maximum:
-//   M = max(lse_c, s_k),  Z = sum_c 2^(lse_c - M) + sum_k 2^(s_k - M),
+// segment that covered (g, b). With M the largest of all lse_c and s_k:
+//   Z = sum_c 2^(lse_c - M) + sum_k 2^(s_k - M),
 //   o = (sum_c 2^(lse_c - M) o_c + sum_k 2^(s_k - M) v_k) / Z,
 //   lse = (M + log2 Z) ln 2          (natural log, as the header promises).
 //
-// Grid: (row blocks of 16, bs * Hkv). The draft K/V rows of (b, g) are staged
-// in shared memory as fp32; each warp then owns two query rows, its lanes own
-// output columns d = lane + 32 e, so every partial read is a coalesced run.
+// One warp per query row (grid: row blocks of 8 x (bs * Hkv)). Lane l owns the
+// output columns [l * VPL, (l + 1) * VPL), so every partial row is read as one
+// coalesced run; the segments' lse values are read lane-parallel first, then
+// the partial rows are streamed with independent loads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -23,9 +24,8 @@
 namespace va {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRowsPerCta = 16;
-constexpr int kMaxCols = 16;   // v_dim / 32 <= 16, i.e. v_dim <= 512
+constexpr int kWarps = 8;
+constexpr int kMaxQk = 576;   // qk_dim <= 18 * 32
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
@@ -45,145 +45,187 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { retu
 template <>
 __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
-    extern __shared__ __align__(16) float dsm[];
-    const int bg = blockIdx.y;
-    const int b = bg / a.hkv, g = bg % a.hkv;
-    const SeqInfo si = a.seq[b];
-    const int rows_b = a.group * si.draft;
-    const int row0 = blockIdx.x * kRowsPerCta;
-    if (row0 >= rows_b) return;
-    const int dqk = a.qk_dim, dv = a.v_dim;
-    float* kd = dsm;                                  // [draft][dqk]
-    float* vd = dsm + (size_t)a.max_draft * dqk;     // [draft][dv]
-    const T* kc = reinterpret_cast<const T*>(a.k_cache);
-    const T* vc = reinterpret_cast<const T*>(a.v_cache);
-    const T* qg = reinterpret_cast<const T*>(a.q);
-    T* og = reinterpret_cast<T*>(a.out);
-
-    // the D_b draft tokens' K/V rows (positions P_b .. P_b + D_b - 1)
-    const int indptr = si.bad ? 0 : __ldg(a.kv_indptr + b);
-    for (int idx = threadIdx.x; idx < si.draft * dqk; idx += kThreads) {
-        const int k = idx / dqk, d = idx % dqk;
-        float v = 0.f;
-        if (!si.bad) {
-            const int64_t slot = token_slot(a, indptr, (int64_t)si.prefix + k);
-            if (slot >= 0) v = to_f32(kc[(slot * a.hkv + g) * a.k_row_stride + d]);
-            else if (d == 0) set_error(a, VA_ERR_BAD_PAGE);
+// VPL consecutive floats of a row, vectorised.
+template <int VPL>
+__device__ __forceinline__ void load_f32(const float* p, float (&v)[VPL]) {
+    if constexpr (VPL % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < VPL; e += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(p + e);
+            v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
         }
-        kd[idx] = v;
-    }
-    for (int idx = threadIdx.x; idx < si.draft * dv; idx += kThreads) {
-        const int k = idx / dv, d = idx % dv;
-        float v = 0.f;
-        if (!si.bad) {
-            const int64_t slot = token_slot(a, indptr, (int64_t)si.prefix + k);
-            if (slot >= 0) v = to_f32(vc[(slot * a.hkv + g) * a.v_row_stride + d]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VPL; e += 2) {
+            const float2 x = *reinterpret_cast<const float2*>(p + e);
+            v[e] = x.x; v[e + 1] = x.y;
         }
-        vd[idx] = v;
-    }
-    __syncthreads();
-
-    // prefix segments that covered (g, b): CTAs c_first .. c_last of the partition
-    const int total_tiles = a.header[kHdrTotalTiles];
-    const int64_t work = (int64_t)a.hkv * total_tiles;
-    int c_first = 0, c_last = -1;
-    if (si.tiles > 0) {
-        const int64_t x0 = (int64_t)g * total_tiles + si.tile_off;
-        c_first = cta_of_tile(x0, work, a.num_ctas);
-        c_last = cta_of_tile(x0 + si.tiles - 1, work, a.num_ctas);
-    }
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ncol = dv / 32;
-    for (int r = row0 + warp; r < row0 + kRowsPerCta && r < rows_b; r += kThreads / 32) {
-        const int i = r / a.group, h = g * a.group + r % a.group;
-        const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + h;
-        if (si.bad) {
-            for (int d = lane; d < dv; d += 32) og[qrow * dv + d] = from_f32<T>(NAN);
-            if (lane == 0) a.lse[qrow] = NAN;
-            continue;
-        }
-        float M = -INFINITY, Z = 0.f;
-        float acc[kMaxCols];
-#pragma unroll
-        for (int e = 0; e < kMaxCols; ++e) acc[e] = 0.f;
-
-        // prefix partials
-        for (int c = c_first; c <= c_last; ++c) {
-            // a CTA whose stream range is empty (more CTAs than tiles) wrote nothing
-            if (cta_start(c + 1, work, a.num_ctas) == cta_start(c, work, a.num_ctas)) continue;
-            const int64_t pr = (int64_t)(g * a.bs + b + c) * a.rows_cap + r;
-            const float lc = a.part_lse[pr];
-            if (lc == -INFINITY) continue;
-            const float* po = a.part_o + pr * dv;
-            if (lc > M) {
-                const float f = exp2f(M - lc);
-                Z *= f;
-#pragma unroll
-                for (int e = 0; e < kMaxCols; ++e) acc[e] *= f;
-                M = lc;
-            }
-            const float w = exp2f(lc - M);
-            Z += w;
-#pragma unroll
-            for (int e = 0; e < kMaxCols; ++e)
-                if (e < ncol) acc[e] = fmaf(w, po[lane + 32 * e], acc[e]);
-        }
-
-        // causal draft block: draft keys k = kmin .. i
-        const int kmin = a.window >= 0 ? (i - a.window > 0 ? i - a.window : 0) : 0;
-        for (int k = kmin; k <= i; ++k) {
-            float part = 0.f;
-            for (int d = lane; d < dqk; d += 32) part = fmaf(to_f32(qg[qrow * dqk + d]), kd[k * dqk + d], part);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            const float s = part * a.scale_log2;
-            if (s > M) {
-                const float f = exp2f(M - s);
-                Z *= f;
-#pragma unroll
-                for (int e = 0; e < kMaxCols; ++e) acc[e] *= f;
-                M = s;
-            }
-            const float w = exp2f(s - M);
-            Z += w;
-#pragma unroll
-            for (int e = 0; e < kMaxCols; ++e)
-                if (e < ncol) acc[e] = fmaf(w, vd[k * dv + lane + 32 * e], acc[e]);
-        }
-
-        const float inv = 1.f / Z;
-#pragma unroll
-        for (int e = 0; e < kMaxCols; ++e)
-            if (e < ncol) og[qrow * dv + lane + 32 * e] = from_f32<T>(acc[e] * inv);
-        if (lane == 0) a.lse[qrow] = (M + __log2f(Z)) * 0.69314718055994531f;
     }
 }
 
-template <typename T>
+template <typename T, int VPL>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
+    pdl_wait();   // partials of the prefix kernel (and the work list) are ready
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int bg = blockIdx.y;
+    const int b = bg / a.hkv, g = bg - b * a.hkv;
+    const SeqInfo si = a.seq[b];
+    const int rows_b = a.group * si.draft;
+    const int r = blockIdx.x * kWarps + warp;
+    if (r >= rows_b) return;
+    const int i = r / a.group, h = g * a.group + (r - i * a.group);
+    const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + h;
+    const int dqk = a.qk_dim;
+    T* og = reinterpret_cast<T*>(a.out) + qrow * (VPL * 32) + lane * VPL;
+    if (si.bad) {
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) og[e] = from_f32<T>(NAN);
+        if (lane == 0) a.lse[qrow] = NAN;
+        return;
+    }
+
+    // ---- the prefix segments that covered (g, b)
+    const int total_tiles = a.header[kHdrTotalTiles];
+    const int64_t work = (int64_t)(a.hkv / a.hg) * total_tiles;
+    int c_first = 0, c_last = -1;
+    if (si.tiles > 0) {
+        const int64_t x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
+        c_first = cta_of_tile(x0, work, a.num_ctas);
+        c_last = cta_of_tile(x0 + si.tiles - 1, work, a.num_ctas);
+    }
+    const int64_t slot0 = partial_slot(a, g, b, 0);   // slot of CTA c is slot0 + c
+
+    // ---- independent loads first: the first 32 segments' lse (lane c), the
+    // draft keys' page-table entries (lane k), the query row
+    auto live = [&](int c) {   // CTA c covered some tile (more CTAs than tiles leaves some idle)
+        return c <= c_last && cta_start(c + 1, work, a.num_ctas) != cta_start(c, work, a.num_ctas);
+    };
+    float lse_mine = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * a.rows_cap + r]
+                                          : -INFINITY;
+    const int kmin = a.window >= 0 ? (i - a.window > 0 ? i - a.window : 0) : 0;
+    const int nkeys = i - kmin + 1;   // <= max_draft <= 32
+    const int indptr = __ldg(a.kv_indptr + b);
+    int64_t row_mine = -1;            // physical (slot, head) row of draft key kmin + lane
+    if (lane < nkeys) {
+        const int64_t slot = token_slot(a, indptr, (int64_t)si.prefix + kmin + lane);
+        if (slot >= 0) row_mine = slot * a.hkv + g;
+        else set_error(a, VA_ERR_BAD_PAGE);
+    }
+    const T* qg = reinterpret_cast<const T*>(a.q) + qrow * dqk;
+    const T* kc = reinterpret_cast<const T*>(a.k_cache);
+    const T* vc = reinterpret_cast<const T*>(a.v_cache);
+    float qv[kMaxQk / 32];
+#pragma unroll
+    for (int e = 0; e < kMaxQk / 32; ++e) qv[e] = (lane + 32 * e < dqk) ? to_f32(qg[lane + 32 * e]) : 0.f;
+
+    // ---- draft scores, four keys' rows in flight at a time (lane k keeps s_k)
+    float s_mine = -INFINITY;
+    for (int k0 = 0; k0 < nkeys; k0 += 4) {
+        float part[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            part[u] = 0.f;
+            const int64_t row = __shfl_sync(0xffffffffu, row_mine, (k0 + u) & 31);
+            if (k0 + u < nkeys && row >= 0) {
+                const T* kr = kc + row * a.k_row_stride;
+#pragma unroll
+                for (int e = 0; e < kMaxQk / 32; ++e)
+                    if (lane + 32 * e < dqk) part[u] = fmaf(qv[e], to_f32(kr[lane + 32 * e]), part[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+            if (lane == k0 + u && k0 + u < nkeys) s_mine = part[u] * a.scale_log2;
+        }
+    }
+
+    // ---- M: the largest term
+    float mx = fmaxf(s_mine, lse_mine);
+    for (int c = c_first + 32 + lane; c <= c_last; c += 32)
+        if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * a.rows_cap + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+
+    // ---- weighted sum of the partial rows
+    float acc[VPL];
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+    float z = 0.f;   // lane-partial sum of weights
+    for (int cb = c_first; cb <= c_last; cb += 32) {
+        const int c = cb + lane;
+        float w = 0.f;
+        if (live(c)) {
+            const float lc = cb == c_first ? lse_mine : a.part_lse[(slot0 + c) * a.rows_cap + r];
+            w = lc == -INFINITY ? 0.f : exp2f(lc - mx);
+        }
+        z += w;
+        const int n = c_last - cb + 1 < 32 ? c_last - cb + 1 : 32;
+        for (int j = 0; j < n; j += 4) {   // four independent row loads in flight
+            float v[4][VPL], wj[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wj[u] = __shfl_sync(0xffffffffu, w, j + u);
+                if (j + u < n && wj[u] != 0.f)
+                    load_f32<VPL>(a.part_o + ((slot0 + cb + j + u) * a.rows_cap + r) * (VPL * 32) +
+                                      lane * VPL, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + u < n && wj[u] != 0.f) {
+#pragma unroll
+                    for (int e = 0; e < VPL; ++e) acc[e] = fmaf(wj[u], v[u][e], acc[e]);
+                }
+        }
+    }
+    // draft keys
+    for (int k = 0; k < nkeys; ++k) {
+        const float sk = __shfl_sync(0xffffffffu, s_mine, k);
+        const int64_t vr = __shfl_sync(0xffffffffu, row_mine, k);
+        const float w = exp2f(sk - mx);
+        if (lane == 0) z += w;
+        if (vr < 0) continue;
+        const T* vp = vc + vr * a.v_row_stride + lane * VPL;
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) acc[e] = fmaf(w, to_f32(vp[e]), acc[e]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) og[e] = from_f32<T>(acc[e] * inv);
+    if (lane == 0) a.lse[qrow] = (mx + __log2f(z)) * 0.69314718055994531f;
+}
+
+template <typename T, int VPL>
 cudaError_t launch_t(const Args& a, cudaStream_t s) {
-    const size_t bytes = (size_t)a.max_draft * (a.qk_dim + a.v_dim) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(combine_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    dim3 grid((a.rows_cap + kRowsPerCta - 1) / kRowsPerCta, a.bs * a.hkv);
-    combine_kernel<T><<<grid, kThreads, bytes, s>>>(a);
-    return cudaGetLastError();
+    dim3 grid((a.rows_cap + kWarps - 1) / kWarps, a.bs * a.hkv);
+    return launch_pdl(combine_kernel<T, VPL>, grid, dim3(kWarps * 32), 0, s, a);
+}
+
+template <typename T>
+cudaError_t launch_dtype(const Args& a, cudaStream_t s) {
+    switch (a.v_dim) {
+    case 64: return launch_t<T, 2>(a, s);
+    case 128: return launch_t<T, 4>(a, s);
+    case 256: return launch_t<T, 8>(a, s);
+    case 512: return launch_t<T, 16>(a, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-size_t combine_smem_bytes(int max_draft, int qk_dim, int v_dim) {
-    return (size_t)max_draft * (qk_dim + v_dim) * sizeof(float);
+bool combine_supported(int qk_dim, int v_dim) {
+    return qk_dim <= kMaxQk && (v_dim == 64 || v_dim == 128 || v_dim == 256 || v_dim == 512);
 }
 
 cudaError_t launch_combine(const Args& a, int dtype, cudaStream_t s) {
     switch (dtype) {
-    case VA_FP32: return launch_t<float>(a, s);
-    case VA_BF16: return launch_t<__nv_bfloat16>(a, s);
-    case VA_FP16: return launch_t<__half>(a, s);
+    case VA_FP32: return launch_dtype<float>(a, s);
+    case VA_BF16: return launch_dtype<__nv_bfloat16>(a, s);
+    case VA_FP16: return launch_dtype<__half>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }

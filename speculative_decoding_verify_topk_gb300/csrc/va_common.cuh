@@ -7,8 +7,9 @@
 //
 //   * The prefix of sequence b that any of its rows can see is [lo_b, P_b),
 //     lo_b = max(0, P_b - window) (row 0 has the lowest window bound). It is
-//     cut into 64-token tiles aligned to absolute positions: tile t covers
-//     [a_b + 64 t, a_b + 64 t + 64), a_b = lo_b rounded down to 64.
+//     cut into TT-token tiles aligned to absolute positions (TT = the plan's
+//     tile_tokens, 64 or 128): tile t covers [a_b + TT t, a_b + TT (t + 1)),
+//     a_b = lo_b rounded down to a multiple of TT.
 //   * The tiles of all (kv-head, sequence) pairs form one stream, kv-head
 //     major: tile x of the stream is (g, b, t) with
 //     x = g * T + tile_off_b + t, T = sum_b tiles_b.
@@ -30,8 +31,8 @@
 
 namespace va {
 
-constexpr int kTile = 64;          // KV tokens per prefix tile
-constexpr int kMaxDraft = 64;      // largest supported num_draft
+constexpr int kTile = 64;          // KV tokens per prefix tile of the fp32 kernel
+constexpr int kMaxDraft = 32;      // largest supported num_draft (one lane per draft key)
 constexpr int kHeaderBytes = 256;  // workspace header: error word, totals
 
 // Header words (int32) at the start of the workspace.
@@ -43,7 +44,7 @@ struct SeqInfo {
     int32_t prefix;    // P_b
     int32_t draft;     // D_b (0 when the sequence failed a check)
     int32_t lo;        // lowest prefix key any row sees: max(0, P_b - window)
-    int32_t a0;        // first tile start: lo rounded down to kTile
+    int32_t a0;        // first tile start: lo rounded down to a multiple of the tile
     int32_t tiles;     // prefix tiles
     int32_t tile_off;  // exclusive prefix sum of tiles
     int32_t bad;       // nonzero: the sequence failed a device check; its rows are NaN
@@ -70,6 +71,8 @@ struct Args {
     int64_t v_row_stride;    // same for V (== K's when V aliases K)
     int bs, hq, hkv, group, qk_dim, v_dim, page_size, window, rows_cap, max_draft;
     int num_ctas;            // persistent CTAs of the prefix kernel
+    int tile;                // KV tokens per prefix tile (the plan's tile_tokens)
+    int hg;                  // kv-heads a prefix CTA handles together (1 on the fp32 path)
     float scale_log2;        // scale * log2(e)
     float scale;
 };
@@ -81,15 +84,45 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
         void* workspace, void* stream, void* const* events);
 
+// Launches `kern` with programmatic stream serialization: it may begin while
+// the preceding kernel on the stream finishes, and must call pdl_wait()
+// before it reads that kernel's results.
+template <typename... KArgs, typename... Act>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
+}
+
+// Shared-memory geometry of a bf16 / fp16 prefix launch (runtime: it depends
+// on the page size and the head grouping); derived from the plan on the host.
+struct Geo {
+    int hg, mt, nc;        // heads per CTA, m16 tiles per head, consumer warps
+    int tb, ppt;           // tokens per TMA box, boxes (page chunks) per tile
+    int box_stride;        // bytes between boxes (box bytes rounded up to 1 KB)
+    int half_bytes;        // one 64-column slice of a tile: ppt * box_stride
+    int nhk, nhv;          // 64-column slices of K and of V rows
+    int stage_bytes, stages;
+    uint32_t tx_box;       // bytes one box delivers
+};
+
 // Host-side launchers (one per translation unit).
 cudaError_t launch_worklist(const Args& a, cudaStream_t s);
-cudaError_t launch_prefix_mma(const Args& a, int dtype, int variant, cudaStream_t s);
 cudaError_t launch_prefix_f32(const Args& a, cudaStream_t s);
 cudaError_t launch_prefix_mla(const Args& a, cudaStream_t s);
 cudaError_t launch_combine(const Args& a, int dtype, cudaStream_t s);
-bool prefix_mma_supported(int qk_dim, int v_dim, int variant);
-int prefix_mma_ctas_per_sm(int qk_dim, int v_dim, int variant);
 size_t prefix_f32_smem_bytes(int qk_dim, int v_dim, int rows_cap);
+bool combine_supported(int qk_dim, int v_dim);
+bool prefix_mma_built(int qk_dim, int v_dim);
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -97,6 +130,16 @@ size_t prefix_f32_smem_bytes(int qk_dim, int v_dim, int rows_cap);
 
 __device__ __forceinline__ void set_error(const Args& a, int bits) {
     atomicOr(a.header + kHdrError, bits);
+}
+
+// Partial-result slot of (kv-head g, sequence b) written by CTA c. The stream
+// runs over (head group, sequence, tile), head group = g / hg; along it,
+// group * bs + b + c strictly increases for a fixed head-in-group g % hg, so
+// slot = (g % hg) * (groups * bs + N) + (g / hg) * bs + b + c is unique and
+// below Hkv * bs + hg * N.
+__device__ __forceinline__ int64_t partial_slot(const Args& a, int g, int b, int c) {
+    const int groups = a.hkv / a.hg, gl = g % a.hg, grp = g / a.hg;
+    return (int64_t)gl * ((int64_t)groups * a.bs + a.num_ctas) + (int64_t)grp * a.bs + b + c;
 }
 
 // First stream tile of persistent CTA c: floor(c * W / N).
@@ -159,6 +202,79 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---- mbarrier / bulk-copy (TMA) / PDL wrappers ---------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+// Makes mbarrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) accesses to the same addresses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Waits for the phase with the given parity to complete. Bounded: after
+// kWaitNs of wall time (far beyond any legitimate wait) it gives up and
+// returns false; the caller then flags VA_ERR_TIMEOUT and winds down.
+constexpr uint64_t kWaitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+// Bulk global->shared copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) that signals completion on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+// Arrives on the mbarrier once all cp.async copies this thread issued so far
+// have landed (the arrival does not raise the expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// Named barrier among `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// allow the next kernel to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 }  // namespace va

@@ -35,6 +35,7 @@ struct F32Layout {
 
 __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
     extern __shared__ __align__(16) unsigned char smem[];
+    pdl_wait();   // the work list is ready from here on
     const int dqk = a.qk_dim, dv = a.v_dim;
     const F32Layout L(dqk, dv, a.rows_cap);
     float* ks = reinterpret_cast<float*>(smem + L.k_off);
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
         }
 
         if (seg_end) {
-            const int slot = cur.g * a.bs + cur.b + cta;
+            const int64_t slot = partial_slot(a, cur.g, cur.b, cta);
             for (int r = warp; r < rows_b; r += kWarps) {
                 const float l = ls[r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -187,8 +188,7 @@ cudaError_t launch_prefix_f32(const Args& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(prefix_f32_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    prefix_f32_kernel<<<a.num_ctas, kThreads, bytes, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prefix_f32_kernel, dim3(a.num_ctas), dim3(kThreads), bytes, s, a);
 }
 
 }  // namespace va

@@ -3,26 +3,41 @@
 //
 // What one CTA computes ("Split-KV flash-decode attention for EAGLE
 // target-verify (Triton backend)", Modifications, the prefix stage): for each
-// segment of its share of the tile stream -- one kv-head g of one sequence b,
-// keys [j_start, j_end) of the prefix -- the normalised partial attention
-// output of the G * D_b query rows that read kv-head g, and its log-sum-exp.
-// Rows are r = i * G + hh (draft i, q-head g * G + hh); the window lower bound
-// of row r is P_b + i - window. Prefix keys j >= P_b (the drafts) are left to
-// the combine kernel.
+// segment of its share of the tile stream -- a group of HG kv-heads of one
+// sequence b, a run of prefix keys -- the normalised partial attention output
+// of the G * D_b query rows of every kv-head g in the group, and its base-2
+// log-sum-exp. Rows of head g are r = i * G + hh (draft i, q-head g * G + hh);
+// row r's window lower bound is P_b + i - window. Keys j >= P_b (the drafts)
+// are left to the combine kernel.
 //
-// GB300 mapping. The path is HBM-bound (16-40 flop per KV byte), so the design
-// goal is bytes in flight: every KV token row of one head is a contiguous
-// qk_dim * 2-byte run somewhere in the pool, gathered with 16-byte cp.async
-// (consecutive lanes, consecutive chunks of one row) into a STAGES-deep
-// shared-memory ring, while the tensor cores (warp-level m16n8k16, fp32
-// accumulate) do QK^T and PV on the previous tiles. Warps split the 64-token
-// tile (WN groups) and the query rows (MT m16 tiles); at a segment's end the
-// WN token groups are merged through the tile's own shared-memory stage.
-// Shared-memory rows use a 16-byte-chunk XOR swizzle so ldmatrix is
-// conflict-free. Physical token slots of a tile are resolved once, a ring
-// step ahead, by 64 threads into shared memory.
+// GB300 mapping. The path is HBM-bound (16-40 flop per KV byte):
+//   * A tile is TT = 16 tokens of one sequence for all HG heads of the group.
+//     In the paged pool [pages, page_size, Hkv, D] a run of tokens inside one
+//     page is one strided box for the tensor memory accelerator: one TMA op
+//     (cp.async.bulk.tensor, 3-d map {D, token slot, head} with the head as
+//     the outer box dimension) brings TB tokens x HG heads x 64 columns
+//     (TB = gcd(page_size, 16)) into shared memory as [head][token][64] with
+//     the 128-byte swizzle, so every ldmatrix phase of one head's rows is
+//     bank-conflict free (for TB >= 8). Requests are 1-16 KB: measured on
+//     GB300, 4 KB boxes stream random pages at ~4.8 TB/s where per-thread
+//     16-byte cp.async tops out near 2.9 TB/s.
+//   * One producer warp walks the tile stream, reads page-table entries two
+//     tiles ahead, and issues the boxes into a STAGES-deep ring whose stages
+//     complete on an mbarrier's transaction count.
+//   * NC = HG * MT consumer warps, one per (head, m16 tile of rows): QK^T and
+//     PV on the tensor cores (warp-level m16n8k16, fp32 accumulate), online
+//     softmax in base 2. A warp owns its head's rows outright, so partial
+//     results need no cross-warp merge; each warp releases the stage with one
+//     arrive. Query fragments are read straight from global memory at the
+//     start of a segment (a few per CTA).
+//   * V rows of tokens at or past P_b may hold another sequence's data or
+//     garbage; in the tiles that reach P_b each consumer zeroes its head's V
+//     rows there before P V (0 * NaN would poison the sum).
+// Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT
+// and the CTA winds down (no further waits) instead of hanging.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -79,361 +94,343 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& d0, uint32_t&
                  : "r"(addr));
 }
 
-// Byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile whose rows
-// hold CH chunks (CH a multiple of 8).
-template <int CH>
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-    return (uint32_t)(row * CH + (ch ^ (row & 7))) * 16u;
+// 3-d tiled TMA load: box at coordinates {col, token slot, head} -> shared.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
 }
 
-template <int DQK, int DV, int MT>
-struct Cfg {
-    static constexpr int WN = MT == 1 ? 4 : 2;      // token groups per tile
-    static constexpr int NW = MT * WN;
-    static constexpr int NT = NW * 32;
-    static constexpr int TPW = kTile / WN;          // tokens per warp per tile
-    static constexpr int NS = TPW / 8;              // score n8 tiles per warp
-    static constexpr int KS = TPW / 16;             // PV k16 steps per warp
-    static constexpr int CK = DQK / 8;              // 16-byte chunks per K row
-    static constexpr int CV = DV / 8;
-    static constexpr int ROWS = 16 * MT;
-    static constexpr int K_BYTES = kTile * DQK * 2;
-    static constexpr int V_BYTES = kTile * DV * 2;
-    static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-    static constexpr int Q_BYTES = ROWS * DQK * 2;
-    static constexpr int MIN_BLOCKS = MT >= 4 ? 1 : 2;
-    static constexpr int BUDGET = (MIN_BLOCKS == 2 ? 113 : 220) * 1024;
-    static constexpr int STAGES =
-        (4 * STAGE_BYTES + Q_BYTES + 4 * 512 <= BUDGET) ? 4
-        : (3 * STAGE_BYTES + Q_BYTES + 3 * 512 <= BUDGET) ? 3 : 2;
-    static constexpr int SLOT_BYTES = STAGES * kTile * 8;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + Q_BYTES + SLOT_BYTES;
-    // merge scratch: per (m-tile, token group > 0) an O tile [16][DV] fp32 in
-    // the finished tile's stage, and 32 floats of (m, l) in the query buffer
-    // (free once the segment's query fragments are in registers)
-    static constexpr int MERGE_UNIT = 16 * DV * 4;
-    static constexpr int MERGE_BYTES = MT * (WN - 1) * MERGE_UNIT;
-    static_assert(MT * (WN - 1) * 32 * 4 <= Q_BYTES, "(m, l) scratch must fit in the query buffer");
-    static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims must be multiples of 64");
-    static_assert(MERGE_BYTES <= STAGE_BYTES, "merge scratch must fit in one stage");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
-};
+constexpr int kTT = 16;            // tokens per tile
+constexpr int kMaxConsumers = 8;   // consumer warps per CTA (HG * MT)
+constexpr int kThreads = (kMaxConsumers + 1) * 32;
 
-template <typename T, int DQK, int DV, int MT>
-__global__ void __launch_bounds__(Cfg<DQK, DV, MT>::NT, Cfg<DQK, DV, MT>::MIN_BLOCKS)
-    prefix_mma_kernel(Args a) {
-    using C = Cfg<DQK, DV, MT>;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char* const stage_base = smem;
-    unsigned char* const q_smem = smem + C::STAGES * C::STAGE_BYTES;
-    int64_t* const slot_smem = reinterpret_cast<int64_t*>(q_smem + C::Q_BYTES);
+template <typename T, int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefix_mma_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, Args a, Geo geo) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1 KB alignment for the 128-byte swizzle atoms
+    unsigned char* const ring =
+        smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* const bars = ring + geo.stages * geo.stage_bytes;
+    const uint32_t bar_full = smem_u32(bars);                 // [stages], count 1 (+ tx)
+    const uint32_t bar_empty = bar_full + 8 * geo.stages;     // [stages], count nc
+    __shared__ int abort_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wm = warp / C::WN, wn = warp % C::WN;
+    if (tid == 0) {
+        for (int s = 0; s < geo.stages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, geo.nc);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp > geo.nc) return;   // launch may round the block up
+
+    pdl_wait();   // the work list (seq table, total tiles) is ready from here on
+
     const int total_tiles = a.header[kHdrTotalTiles];
-    const int64_t work = (int64_t)a.hkv * total_tiles;
+    const int n_groups = a.hkv / a.hg;
+    const int64_t work = (int64_t)n_groups * total_tiles;
     const int cta = blockIdx.x;
     const int64_t x_begin = cta_start(cta, work, a.num_ctas);
-    const int64_t x_end = cta_start(cta + 1, work, a.num_ctas);
-    const int n_tiles = (int)(x_end - x_begin);
-    if (n_tiles <= 0) return;
-
-    const T* __restrict__ kc = reinterpret_cast<const T*>(a.k_cache);
-    const T* __restrict__ vc = reinterpret_cast<const T*>(a.v_cache);
-    const T* __restrict__ qg = reinterpret_cast<const T*>(a.q);
-
-    // ---- physical rows of a tile's tokens (threads < 64), one ring step ahead
-    Cursor slot_cur;
-    slot_cur.seek(a, x_begin, total_tiles);
-    auto resolve_slots = [&](int k) {  // tile k of this CTA, k == slot_tile
-        if (k < n_tiles) {
-            if (tid < kTile) {
-                const SeqInfo si = a.seq[slot_cur.b];
-                const int64_t j = (int64_t)si.a0 + (int64_t)slot_cur.t * kTile + tid;
-                int64_t row = -1;
-                if (j >= si.lo && j < si.prefix) {
-                    const int64_t slot = token_slot(a, __ldg(a.kv_indptr + slot_cur.b), j);
-                    if (slot >= 0) row = slot * a.hkv + slot_cur.g;
-                    else set_error(a, VA_ERR_BAD_PAGE);
-                }
-                slot_smem[(k % C::STAGES) * kTile + tid] = row;
-            }
-            if (k + 1 < n_tiles) slot_cur.advance(a);
-        }
-    };
-    auto issue_loads = [&](int k) {  // tile k into stage k % STAGES
-        if (k < n_tiles) {
-            const int st = k % C::STAGES;
-            const uint32_t kdst = smem_u32(stage_base + st * C::STAGE_BYTES);
-            const uint32_t vdst = kdst + C::K_BYTES;
-            const int64_t* rows = slot_smem + st * kTile;
-#pragma unroll 4
-            for (int idx = tid; idx < kTile * C::CK; idx += C::NT) {
-                const int tok = idx / C::CK, ch = idx % C::CK;
-                const int64_t r = rows[tok];
-                const T* src = r >= 0 ? kc + r * a.k_row_stride + ch * 8 : kc;
-                cp_async16(kdst + swz<C::CK>(tok, ch), src, r >= 0 ? 16 : 0);
-            }
-#pragma unroll 4
-            for (int idx = tid; idx < kTile * C::CV; idx += C::NT) {
-                const int tok = idx / C::CV, ch = idx % C::CV;
-                const int64_t r = rows[tok];
-                const T* src = r >= 0 ? vc + r * a.v_row_stride + ch * 8 : vc;
-                cp_async16(vdst + swz<C::CV>(tok, ch), src, r >= 0 ? 16 : 0);
-            }
-        }
-        cp_async_commit();
-    };
-
-    // pipeline prologue: slots of tiles 0 .. STAGES-1, loads of tiles 0 .. STAGES-2
-    for (int k = 0; k < C::STAGES; ++k) resolve_slots(k);
-    __syncthreads();
-    for (int k = 0; k < C::STAGES - 1; ++k) issue_loads(k);
-
+    const int n_tiles = (int)(cta_start(cta + 1, work, a.num_ctas) - x_begin);
+    if (n_tiles <= 0) {
+        pdl_launch_dependents();
+        return;
+    }
     Cursor cur;
-    cur.seek(a, x_begin, total_tiles);
+    cur.seek(a, x_begin, total_tiles);   // cur.g is the head group
 
-    uint32_t qf[DQK / 16][4];
-    float o[DV / 8][4];
-    float m_run[2], l_run[2];
-    int seg_b = -1, seg_g = -1;
-    SeqInfo si = {};
-    int rows_b = 0, lo_r[2] = {0, 0};
-
-    for (int k = 0; k < n_tiles; ++k) {
-        cp_async_wait<C::STAGES - 2>();
-        __syncthreads();
-        issue_loads(k + C::STAGES - 1);
-        resolve_slots(k + C::STAGES);
-
-        const bool seg_begin = (k == 0) || (cur.t == 0);
-        const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
-
-        if (seg_begin) {
-            seg_b = cur.b;
-            seg_g = cur.g;
-            si = a.seq[seg_b];
-            rows_b = a.group * si.draft;
-            // query rows of (b, g) -> shared memory (zero rows past rows_b)
-            for (int idx = tid; idx < C::ROWS * C::CK; idx += C::NT) {
-                const int row = idx / C::CK, ch = idx % C::CK;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (row < rows_b) {
-                    const int i = row / a.group, hh = row % a.group;
-                    const int64_t qrow = ((int64_t)(si.qoff + i) * a.hq + seg_g * a.group + hh);
-                    v = __ldg(reinterpret_cast<const uint4*>(qg + qrow * DQK + ch * 8));
+    if (warp == geo.nc) {
+        // =================== producer warp ===================
+        // Lane c < ppt owns page chunk c of a tile. Its page-table read for
+        // tile k + 2 is issued in iteration k and used in iteration k + 1.
+        Cursor ahead = cur;
+        int cached_b = -1, s_a0 = 0, s_lo = 0, s_prefix = 0, s_indptr = 0;
+        int p_page = -1, p_off = 0;         // pending (tile k + 1): page id, first slot offset
+        bool p_valid = false;
+        int n_page = -1, n_off = 0;         // tile being issued (k)
+        bool n_valid = false;
+        auto start = [&]() {
+            if (ahead.b != cached_b) {
+                const SeqInfo si = a.seq[ahead.b];
+                s_a0 = si.a0; s_lo = si.lo; s_prefix = si.prefix;
+                s_indptr = __ldg(a.kv_indptr + ahead.b);
+                cached_b = ahead.b;
+            }
+            const int jc = s_a0 + ahead.t * kTT + lane * geo.tb;   // first token of chunk `lane`
+            p_valid = lane < geo.ppt && jc < s_prefix && jc + geo.tb > s_lo;
+            p_off = jc % a.page_size;
+            p_page = p_valid ? __ldg(a.page_table + s_indptr + jc / a.page_size) : -1;
+        };
+        start();
+        n_page = p_page; n_off = p_off; n_valid = p_valid;
+        if (n_tiles > 1) {
+            ahead.advance(a);
+            start();
+        }
+        const int nparts = geo.nhk + geo.nhv;
+        const int n_ops = geo.ppt * nparts;
+        for (int k = 0; k < n_tiles; ++k) {
+            const int st = k % geo.stages;
+            if (k >= geo.stages && !*(volatile int*)&abort_flag &&
+                !mbar_wait(bar_empty + 8 * st, ((k / geo.stages) - 1) & 1)) {
+                set_error(a, VA_ERR_TIMEOUT);
+                abort_flag = 1;
+            }
+            // chunk validity / page range, then the stage's byte count
+            bool ok = n_valid;
+            if (ok && (n_page < 0 || n_page >= a.num_pages)) {
+                ok = false;
+                set_error(a, VA_ERR_BAD_PAGE);
+            }
+            const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+            const uint32_t full = bar_full + 8 * st;
+            if (lane == 0)
+                mbar_arrive_expect_tx(full, (uint32_t)__popc(okmask) * nparts * geo.tx_box);
+            __syncwarp();
+            const uint32_t sbase = smem_u32(ring + st * geo.stage_bytes);
+            for (int op0 = 0; op0 < n_ops; op0 += 32) {   // whole-warp rounds (for the shuffles)
+                const int op = op0 + lane;
+                const int c = (op < n_ops ? op : 0) / nparts;
+                const int page = __shfl_sync(0xffffffffu, n_page, c);
+                const int off = __shfl_sync(0xffffffffu, n_off, c);
+                if (op >= n_ops || !((okmask >> c) & 1u)) continue;
+                const int part = op - c * nparts;
+                const int slot = page * a.page_size + off;
+                const uint32_t dst = sbase + part * geo.half_bytes + c * geo.box_stride;
+                if (part < geo.nhk)
+                    tma_load_3d(dst, &kmap, part * 64, slot, cur.g * geo.hg, full);
+                else
+                    tma_load_3d(dst, &vmap, (part - geo.nhk) * 64, slot, cur.g * geo.hg, full);
+            }
+            if (k + 1 < n_tiles) {
+                n_page = p_page; n_off = p_off; n_valid = p_valid;
+                if (k + 2 < n_tiles) {
+                    ahead.advance(a);
+                    start();
                 }
-                *reinterpret_cast<uint4*>(q_smem + swz<C::CK>(row, ch)) = v;
+                cur.advance(a);
             }
-            __syncthreads();
-            {
-                const int mi = lane >> 3, r8 = lane & 7;
-                const int row = wm * 16 + (mi & 1) * 8 + r8;
-#pragma unroll
-                for (int kk = 0; kk < DQK / 16; ++kk)
-                    ldsm_x4(smem_u32(q_smem + swz<C::CK>(row, kk * 2 + (mi >> 1))), qf[kk][0],
-                            qf[kk][1], qf[kk][2], qf[kk][3]);
+        }
+        // Normally the consumers wait for every fill, so nothing is in flight
+        // at exit. After an abort, wait (bounded) for the last fill of each stage.
+        if (*(volatile int*)&abort_flag) {
+            const int k0 = n_tiles - geo.stages > 0 ? n_tiles - geo.stages : 0;
+            for (int k = k0; k < n_tiles; ++k)
+                mbar_wait(bar_full + 8 * (k % geo.stages), (k / geo.stages) & 1);
+        }
+    } else {
+        // =================== consumer warps ===================
+        const int gl = warp / geo.mt, wm = warp - gl * geo.mt;   // head in group, m16 tile
+        const int mi = lane >> 3, r8 = lane & 7;
+        uint32_t qf[DQK / 16][4];
+        float o[DV / 8][4];
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        int rows_b = 0, lo_r[2] = {0, 0};
+        SeqInfo si = {};
+        auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+            if (*(volatile int*)&abort_flag) return;
+            if (!mbar_wait(bar, parity)) {
+                set_error(a, VA_ERR_TIMEOUT);
+                abort_flag = 1;
             }
+        };
+        const T* __restrict__ qg = reinterpret_cast<const T*>(a.q);
+        // byte offset of 16-byte chunk ch (0..7) of token t (0..15) of this
+        // warp's head inside one 64-column half of a stage
+        auto rowaddr = [&](int t, int ch) -> uint32_t {
+            const int c = t / geo.tb, rr = gl * geo.tb + (t - c * geo.tb);   // row inside the box
+            return (uint32_t)(c * geo.box_stride + rr * 128 + ((ch ^ (rr & 7)) << 4));
+        };
+
+        for (int k = 0; k < n_tiles; ++k) {
+            const int st = k % geo.stages;
+            const bool seg_begin = (k == 0) || (cur.t == 0);
+            const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
+            const int g = cur.g * geo.hg + gl;   // this warp's kv-head
+            if (seg_begin) {
+                si = a.seq[cur.b];
+                rows_b = a.group * si.draft;
+                // query A fragments of rows wm*16 + lane/4 (+ 8), straight from global
+                const int c2 = 2 * (lane & 3);
 #pragma unroll
-            for (int n = 0; n < DV / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            m_run[0] = m_run[1] = -INFINITY;
-            l_run[0] = l_run[1] = 0.f;
-            {
-                const int r0 = wm * 16 + (lane >> 2);
                 for (int h = 0; h < 2; ++h) {
-                    const int i = (r0 + 8 * h) / a.group;
+                    const int r = wm * 16 + (lane >> 2) + 8 * h;
+                    const T* qrow = qg;
+                    const bool live = r < rows_b;
+                    if (live) {
+                        const int i = r / a.group, hh = r - i * a.group;
+                        qrow = qg + ((int64_t)(si.qoff + i) * a.hq + g * a.group + hh) * DQK;
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < DQK / 16; ++kk) {
+                        qf[kk][h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + c2)) : 0u;
+                        qf[kk][2 + h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 8 + c2)) : 0u;
+                    }
+                }
+#pragma unroll
+                for (int n = 0; n < DV / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+                m_run[0] = m_run[1] = -INFINITY;
+                l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i = (wm * 16 + (lane >> 2) + 8 * h) / a.group;
                     lo_r[h] = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
                 }
             }
-        }
+            wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
+            unsigned char* const stage = ring + st * geo.stage_bytes;
+            const uint32_t kbase = smem_u32(stage);
+            const uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
+            const int tile_j0 = si.a0 + cur.t * kTT;
 
-        // ---- S = Q K^T for this warp's TPW tokens
-        const int st = k % C::STAGES;
-        const unsigned char* ks = stage_base + st * C::STAGE_BYTES;
-        const unsigned char* vs = ks + C::K_BYTES;
-        float s[C::NS][4];
+            // V rows of tokens at or past the prefix end: zero them (this head)
+            const bool tail = tile_j0 + kTT > si.prefix;
+            if (tail) {
+                for (int idx = lane; idx < kTT * geo.nhv * 8; idx += 32) {
+                    const int t = idx / (geo.nhv * 8), rem = idx - t * geo.nhv * 8;
+                    const int h = rem >> 3, ch = rem & 7;
+                    if (tile_j0 + t >= si.prefix)
+                        *reinterpret_cast<uint4*>(stage + (geo.nhk + h) * geo.half_bytes + rowaddr(t, ch)) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // ---- S = Q K^T over the tile's 16 tokens (two n8 tiles)
+            float s[2][4];
 #pragma unroll
-        for (int n = 0; n < C::NS; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-        {
-            const int mi = lane >> 3, r8 = lane & 7;
+            for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
+                const int tok = (mi >> 1) * 8 + r8;
+                const int ch = (kk & 3) * 2 + (mi & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + (kk >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
+                Mma<T>::run(s[0], qf[kk], b0, b1);
+                Mma<T>::run(s[1], qf[kk], b2, b3);
+            }
+
+            // ---- scale, mask, online softmax (rows lane/4 and lane/4 + 8 of the m-tile)
+            const bool need_mask = tail ||
+                                   (a.window >= 0 && tile_j0 < si.prefix + si.draft - 1 - a.window);
+            const int j_base = tile_j0 + 2 * (lane & 3);
+            float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int np = 0; np < C::NS / 2; ++np) {
-                    const int tok = wn * C::TPW + np * 16 + (mi >> 1) * 8 + r8;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(ks + swz<C::CK>(tok, kk * 2 + (mi & 1))), b0, b1, b2, b3);
-                    Mma<T>::run(s[2 * np], qf[kk], b0, b1);
-                    Mma<T>::run(s[2 * np + 1], qf[kk], b2, b3);
+            for (int n = 0; n < 2; ++n) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = s[n][e] * a.scale_log2;
+                    if (need_mask) {
+                        const int j = j_base + n * 8 + (e & 1);
+                        if (j >= si.prefix || j < lo_r[e >> 1]) v = -INFINITY;
+                    }
+                    s[n][e] = v;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
                 }
             }
-        }
-
-        // ---- scale, mask, online softmax (rows r0 = lane/4 and r0 + 8 of the m-tile)
-        // a tile needs masking if it reaches past the prefix or starts below the
-        // highest window bound of any row (P_b + D_b - 1 - window)
-        const int tile_j0 = si.a0 + cur.t * kTile;
-        const bool need_mask = (tile_j0 + kTile > si.prefix) ||
-                               (a.window >= 0 && tile_j0 < si.prefix + si.draft - 1 - a.window);
-        const int j_tile = tile_j0 + wn * C::TPW;
-        float mx[2] = {-INFINITY, -INFINITY};
+            float alpha[2], m_use[2];
 #pragma unroll
-        for (int n = 0; n < C::NS; ++n) {
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                const float m_new = fmaxf(m_run[h], mx[h]);
+                m_use[h] = m_new == -INFINITY ? 0.f : m_new;
+                alpha[h] = exp2f(m_run[h] - m_use[h]);
+                m_run[h] = m_new;
+            }
+            float psum[2] = {0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = s[n][e] * a.scale_log2;
-                if (need_mask) {
-                    const int j = j_tile + n * 8 + 2 * (lane & 3) + (e & 1);
-                    if (j >= si.prefix || j < lo_r[e >> 1]) v = -INFINITY;
+            for (int n = 0; n < 2; ++n) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p = exp2f(s[n][e] - m_use[e >> 1]);
+                    s[n][e] = p;
+                    psum[e >> 1] += p;
                 }
-                s[n][e] = v;
-                mx[e >> 1] = fmaxf(mx[e >> 1], v);
             }
-        }
-        float alpha[2], m_use[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-            const float m_new = fmaxf(m_run[h], mx[h]);
-            m_use[h] = m_new == -INFINITY ? 0.f : m_new;
-            alpha[h] = exp2f(m_run[h] - m_use[h]);
-            m_run[h] = m_new;
-        }
-        float psum[2] = {0.f, 0.f};
+            for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + psum[h];
 #pragma unroll
-        for (int n = 0; n < C::NS; ++n) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p = exp2f(s[n][e] - m_use[e >> 1]);
-                s[n][e] = p;
-                psum[e >> 1] += p;
+            for (int n = 0; n < DV / 8; ++n) {
+                o[n][0] *= alpha[0];
+                o[n][1] *= alpha[0];
+                o[n][2] *= alpha[1];
+                o[n][3] *= alpha[1];
             }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + psum[h];
-#pragma unroll
-        for (int n = 0; n < DV / 8; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
-        }
 
-        // ---- O += P V
-        {
-            const int mi = lane >> 3, r8 = lane & 7;
-#pragma unroll
-            for (int kk = 0; kk < C::KS; ++kk) {
+            // ---- O += P V
+            {
                 uint32_t pa[4];
-                pa[0] = Mma<T>::pack(s[2 * kk][0], s[2 * kk][1]);
-                pa[1] = Mma<T>::pack(s[2 * kk][2], s[2 * kk][3]);
-                pa[2] = Mma<T>::pack(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                pa[3] = Mma<T>::pack(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-                const int tok = wn * C::TPW + kk * 16 + (mi & 1) * 8 + r8;
+                pa[0] = Mma<T>::pack(s[0][0], s[0][1]);
+                pa[1] = Mma<T>::pack(s[0][2], s[0][3]);
+                pa[2] = Mma<T>::pack(s[1][0], s[1][1]);
+                pa[3] = Mma<T>::pack(s[1][2], s[1][3]);
+                const int tok = (mi & 1) * 8 + r8;
 #pragma unroll
                 for (int nd = 0; nd < DV / 16; ++nd) {
+                    const int ch = (nd & 3) * 2 + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(vs + swz<C::CV>(tok, nd * 2 + (mi >> 1))), b0, b1, b2, b3);
+                    ldsm_x4_t(vbase + (nd >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
                     Mma<T>::run(o[2 * nd], pa, b0, b1);
                     Mma<T>::run(o[2 * nd + 1], pa, b2, b3);
                 }
             }
-        }
+            // release the stage; zeroed rows (generic writes) are ordered before
+            // the next fill's bulk-tensor writes
+            if (tail) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
 
-        if (seg_end) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-                l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-            }
-            // merge the WN token groups of each m-tile through this tile's stage
-            __syncthreads();
-            unsigned char* scratch = stage_base + st * C::STAGE_BYTES;
-            const int r0 = lane >> 2, c0 = 2 * (lane & 3);
-            if (wn > 0) {
-                float* ob = reinterpret_cast<float*>(scratch + (wm * (C::WN - 1) + (wn - 1)) * C::MERGE_UNIT);
-                float* ml = reinterpret_cast<float*>(q_smem) + (wm * (C::WN - 1) + (wn - 1)) * 32;
-#pragma unroll
-                for (int n = 0; n < DV / 8; ++n) {
-                    *reinterpret_cast<float2*>(ob + r0 * DV + n * 8 + c0) = make_float2(o[n][0], o[n][1]);
-                    *reinterpret_cast<float2*>(ob + (r0 + 8) * DV + n * 8 + c0) = make_float2(o[n][2], o[n][3]);
-                }
-                if ((lane & 3) == 0) {
-                    ml[r0] = m_run[0];
-                    ml[r0 + 8] = m_run[1];
-                    ml[16 + r0] = l_run[0];
-                    ml[16 + r0 + 8] = l_run[1];
-                }
-            }
-            __syncthreads();
-            if (wn == 0) {
-                float f_self[2], f_w[C::WN > 1 ? C::WN - 1 : 1][2], m_tot[2], l_tot[2];
+            if (seg_end) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    m_tot[h] = m_run[h];
-#pragma unroll
-                    for (int w = 1; w < C::WN; ++w) {
-                        const float* ml = reinterpret_cast<const float*>(q_smem) + (wm * (C::WN - 1) + (w - 1)) * 32;
-                        m_tot[h] = fmaxf(m_tot[h], ml[r0 + 8 * h]);
-                    }
-                    const float mu = m_tot[h] == -INFINITY ? 0.f : m_tot[h];
-                    f_self[h] = exp2f(m_run[h] - mu);
-                    l_tot[h] = l_run[h] * f_self[h];
-#pragma unroll
-                    for (int w = 1; w < C::WN; ++w) {
-                        const float* ml = reinterpret_cast<const float*>(q_smem) + (wm * (C::WN - 1) + (w - 1)) * 32;
-                        f_w[w - 1][h] = exp2f(ml[r0 + 8 * h] - mu);
-                        l_tot[h] += ml[16 + r0 + 8 * h] * f_w[w - 1][h];
-                    }
+                    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+                    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
                 }
-                const float inv0 = l_tot[0] > 0.f ? 1.f / l_tot[0] : 0.f;
-                const float inv1 = l_tot[1] > 0.f ? 1.f / l_tot[1] : 0.f;
-                const int slot = seg_g * a.bs + seg_b + cta;
+                const int r0 = lane >> 2, c0 = 2 * (lane & 3);
+                const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+                const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+                const int64_t slot = partial_slot(a, g, cur.b, cta);
                 const int rr0 = wm * 16 + r0, rr1 = rr0 + 8;
                 float* po = a.part_o + (int64_t)slot * a.rows_cap * DV;
 #pragma unroll
                 for (int n = 0; n < DV / 8; ++n) {
-                    float v0 = o[n][0] * f_self[0], v1 = o[n][1] * f_self[0];
-                    float v2 = o[n][2] * f_self[1], v3 = o[n][3] * f_self[1];
-#pragma unroll
-                    for (int w = 1; w < C::WN; ++w) {
-                        const float* ob = reinterpret_cast<const float*>(
-                            scratch + (wm * (C::WN - 1) + (w - 1)) * C::MERGE_UNIT);
-                        const float2 x0 = *reinterpret_cast<const float2*>(ob + r0 * DV + n * 8 + c0);
-                        const float2 x1 = *reinterpret_cast<const float2*>(ob + (r0 + 8) * DV + n * 8 + c0);
-                        v0 += x0.x * f_w[w - 1][0];
-                        v1 += x0.y * f_w[w - 1][0];
-                        v2 += x1.x * f_w[w - 1][1];
-                        v3 += x1.y * f_w[w - 1][1];
-                    }
                     if (rr0 < rows_b)
                         *reinterpret_cast<float2*>(po + (int64_t)rr0 * DV + n * 8 + c0) =
-                            make_float2(v0 * inv0, v1 * inv0);
+                            make_float2(o[n][0] * inv0, o[n][1] * inv0);
                     if (rr1 < rows_b)
                         *reinterpret_cast<float2*>(po + (int64_t)rr1 * DV + n * 8 + c0) =
-                            make_float2(v2 * inv1, v3 * inv1);
+                            make_float2(o[n][2] * inv1, o[n][3] * inv1);
                 }
                 if ((lane & 3) == 0) {
                     float* pl = a.part_lse + (int64_t)slot * a.rows_cap;
-                    if (rr0 < rows_b) pl[rr0] = l_tot[0] > 0.f ? m_tot[0] + __log2f(l_tot[0]) : -INFINITY;
-                    if (rr1 < rows_b) pl[rr1] = l_tot[1] > 0.f ? m_tot[1] + __log2f(l_tot[1]) : -INFINITY;
+                    if (rr0 < rows_b) pl[rr0] = l_run[0] > 0.f ? m_run[0] + __log2f(l_run[0]) : -INFINITY;
+                    if (rr1 < rows_b) pl[rr1] = l_run[1] > 0.f ? m_run[1] + __log2f(l_run[1]) : -INFINITY;
                 }
             }
+            if (k + 1 < n_tiles) cur.advance(a);
         }
-        if (k + 1 < n_tiles) cur.advance(a);
     }
-    cp_async_wait<0>();
+    pdl_launch_dependents();
 }
 
-template <typename T, int DQK, int DV, int MT>
-cudaError_t launch(const Args& a, cudaStream_t s) {
-    using C = Cfg<DQK, DV, MT>;
-    auto kern = prefix_mma_kernel<T, DQK, DV, MT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+template <typename T, int DQK, int DV>
+cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, const Geo& g,
+                   cudaStream_t s) {
+    auto kern = prefix_mma_kernel<T, DQK, DV>;
+    const int smem = 1024 + g.stages * g.stage_bytes + 16 * g.stages;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<a.num_ctas, C::NT, C::SMEM, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + 1) * 32), smem, s, kmap, vmap, a, g);
 }
 
 }  // namespace mma_path

@@ -3,14 +3,10 @@
 
 namespace va {
 
-cudaError_t launch_prefix_mma_256x256(const Args& a, int dtype, int mt, cudaStream_t s) {
-    using namespace mma_path;
-    const bool bf16 = dtype == VA_BF16;
-    switch (mt) {
-    case 1: return bf16 ? launch<__nv_bfloat16, 256, 256, 1>(a, s) : launch<__half, 256, 256, 1>(a, s);
-    case 2: return bf16 ? launch<__nv_bfloat16, 256, 256, 2>(a, s) : launch<__half, 256, 256, 2>(a, s);
-    default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_prefix_mma_256x256(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                        const Args& a, const Geo& g, int dtype, cudaStream_t s) {
+    return dtype == VA_BF16 ? mma_path::launch<__nv_bfloat16, 256, 256>(kmap, vmap, a, g, s)
+                            : mma_path::launch<__half, 256, 256>(kmap, vmap, a, g, s);
 }
 
 }  // namespace va

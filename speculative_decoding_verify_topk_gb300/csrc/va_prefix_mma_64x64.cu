@@ -3,16 +3,10 @@
 
 namespace va {
 
-cudaError_t launch_prefix_mma_64x64(const Args& a, int dtype, int mt, cudaStream_t s) {
-    using namespace mma_path;
-    const bool bf16 = dtype == VA_BF16;
-    switch (mt) {
-    case 1: return bf16 ? launch<__nv_bfloat16, 64, 64, 1>(a, s) : launch<__half, 64, 64, 1>(a, s);
-    case 2: return bf16 ? launch<__nv_bfloat16, 64, 64, 2>(a, s) : launch<__half, 64, 64, 2>(a, s);
-    case 3: return bf16 ? launch<__nv_bfloat16, 64, 64, 3>(a, s) : launch<__half, 64, 64, 3>(a, s);
-    case 4: return bf16 ? launch<__nv_bfloat16, 64, 64, 4>(a, s) : launch<__half, 64, 64, 4>(a, s);
-    default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_prefix_mma_64x64(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                        const Args& a, const Geo& g, int dtype, cudaStream_t s) {
+    return dtype == VA_BF16 ? mma_path::launch<__nv_bfloat16, 64, 64>(kmap, vmap, a, g, s)
+                            : mma_path::launch<__half, 64, 64>(kmap, vmap, a, g, s);
 }
 
 }  // namespace va

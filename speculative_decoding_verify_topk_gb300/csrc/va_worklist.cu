@@ -46,6 +46,7 @@ __device__ int block_exclusive_scan(int v, int* excl, int* warp_sums) {
 
 __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
     __shared__ int warp_sums[33];
+    pdl_launch_dependents();   // the prefix kernel may start its set-up now
     if (threadIdx.x == 0) a.header[kHdrError] = 0;
     __syncthreads();
 
@@ -75,8 +76,8 @@ __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
             if (!bad && qrows > 0) {
                 const int lo = (a.window >= 0 && p - a.window > 0) ? p - a.window : 0;
                 si.lo = lo;
-                si.a0 = lo & ~(kTile - 1);
-                tiles = p > lo ? (p - si.a0 + kTile - 1) / kTile : 0;
+                si.a0 = lo - lo % a.tile;
+                tiles = p > lo ? (p - si.a0 + a.tile - 1) / a.tile : 0;
             }
             si.tiles = tiles;
         }

@@ -75,13 +75,20 @@ def _plan(**kw):
 def test_plan_selects_paths(lib):
     p = _plan()
     assert p.path == va.VA_PATH_MMA and p.variant == 1 and p.rows_cap == 16
-    assert p.num_ctas == 152 * 2
-    assert p.num_slots == 8 * 16 + p.num_ctas
+    assert p.num_ctas == 152 and p.tile_tokens == 16    # one warp-specialised CTA per SM
+    # 8 kv-heads per CTA (one consumer warp each), boxes of gcd(page_size, 16) = 4 tokens
+    assert p.heads_per_cta == 8 and p.box_tokens == 4 and p.stages >= 3
+    assert p.stage_bytes == (2 + 2) * 4 * (4 * 8 * 128)      # (K + V slices) x boxes x box bytes
+    assert p.num_slots == 8 * 16 + p.heads_per_cta * p.num_ctas
     assert p.workspace_bytes % 256 == 0 and p.workspace_bytes >= (
         p.off_part_o + 4 * p.num_slots * p.rows_cap * 128)
     assert _plan(dtype=va.VA_FP32, qk_dim=64, v_dim=64, num_q_heads=4, num_kv_heads=2).path == va.VA_PATH_F32
-    mixed = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128)
+    mixed = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128,
+                  page_size=16)
     assert mixed.path == va.VA_PATH_MMA and mixed.variant == 3  # 40 rows -> 3 m16 tiles
+    assert mixed.heads_per_cta == 2 and mixed.box_tokens == 16  # 2 heads x 3 tiles = 6 warps
+    assert _plan(page_size=1).box_tokens == 1 and _plan(page_size=64).box_tokens == 16
+    assert _plan(page_size=6).box_tokens == 2
     assert _plan(num_ctas=7).num_ctas == 7
 
 
@@ -94,7 +101,7 @@ def test_workspace_depends_on_max_bs_only(lib):
 @pytest.mark.parametrize("kw", [dict(num_q_heads=30, num_kv_heads=8), dict(max_draft=0),
                                 dict(max_bs=0), dict(page_size=0), dict(dtype=7),
                                 dict(v_aliases_k=True, qk_dim=64, v_dim=128),
-                                dict(max_draft=65), dict(num_pages=0)])
+                                dict(max_draft=33), dict(num_pages=0)])
 def test_plan_rejects_invalid(lib, kw):
     with pytest.raises(va.VerifyAttnError) as e:
         _plan(**kw)
