@@ -108,7 +108,7 @@ def test_plan_rejects_invalid(lib, kw):
     assert e.value.status == binding.VA_INVALID_ARG
 
 
-@pytest.mark.parametrize("kw", [dict(qk_dim=96, v_dim=96), dict(num_q_heads=128, num_kv_heads=8,
+@pytest.mark.parametrize("kw", [dict(qk_dim=96, v_dim=96), dict(num_q_heads=128, num_kv_heads=4,
                                                                 max_draft=8)])
 def test_plan_reports_unsupported(lib, kw):
     with pytest.raises(va.VerifyAttnError) as e:
