@@ -1,21 +1,19 @@
-// Fused combine: the causal draft x draft block plus the log-sum-exp merge of
-// the prefix partials ("Split-KV flash-decode attention for EAGLE
-// target-verify (Triton backend)", Modifications: the combine stage merges the
-// prefix splits and handles the small causal draft-draft block).
+// Combine: the log-sum-exp merge of the split-KV partials ("Split-KV
+// flash-decode attention for EAGLE target-verify (Triton backend)",
+// Modifications: the combine stage merges the prefix splits). The causal
+// draft x draft block is computed by the prefix kernel inside each sequence's
+// last tile (row i sees keys up to P_b + i), so every term arrives here as a
+// partial (lse_c, o_c) from one segment of the split.
 //
-// For query row (b, i, h) -- position p = P_b + i, kv-head g = h / G -- the
-// draft keys it sees are the cache positions P_b + k for
-// max(0, i - window) <= k <= i (all k <= i without a window). Their scores are
-// exact dot products here; the prefix contributes one (lse_c, o_c) pair per
-// segment that covered (g, b). With M the largest of all lse_c and s_k:
-//   Z = sum_c 2^(lse_c - M) + sum_k 2^(s_k - M),
-//   o = (sum_c 2^(lse_c - M) o_c + sum_k 2^(s_k - M) v_k) / Z,
+// For query row (b, i, h), kv-head g = h / G, with M the largest lse_c
+// (base 2) over the segments c that covered (g, b):
+//   Z = sum_c 2^(lse_c - M),  o = sum_c 2^(lse_c - M) o_c / Z,
 //   lse = (M + log2 Z) ln 2          (natural log, as the header promises).
 //
 // One warp per query row (grid: row blocks of 8 x (bs * Hkv)). Lane l owns the
 // output columns [l * VPL, (l + 1) * VPL), so every partial row is read as one
 // coalesced run; the segments' lse values are read lane-parallel first, then
-// the partial rows are streamed with independent loads.
+// the partial rows are streamed four at a time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -25,16 +23,6 @@ namespace va {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kMaxQk = 576;   // qk_dim <= 18 * 32
-
-template <typename T>
-__device__ __forceinline__ float to_f32(T v);
-template <>
-__device__ __forceinline__ float to_f32<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-template <>
-__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
@@ -63,6 +51,8 @@ __device__ __forceinline__ void load_f32(const float* p, float (&v)[VPL]) {
     }
 }
 
+// QPL = qk_dim / 32 query / key elements per lane, VPL = v_dim / 32 output
+// columns per lane (compile-time: the loops below carry no predicates).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     pdl_wait();   // partials of the prefix kernel (and the work list) are ready
@@ -75,74 +65,31 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     if (r >= rows_b) return;
     const int i = r / a.group, h = g * a.group + (r - i * a.group);
     const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + h;
-    const int dqk = a.qk_dim;
     T* og = reinterpret_cast<T*>(a.out) + qrow * (VPL * 32) + lane * VPL;
-    if (si.bad) {
+    if (si.bad || si.tiles == 0) {
 #pragma unroll
         for (int e = 0; e < VPL; ++e) og[e] = from_f32<T>(NAN);
         if (lane == 0) a.lse[qrow] = NAN;
         return;
     }
 
-    // ---- the prefix segments that covered (g, b)
+    // ---- the segments that covered (g, b): CTAs c_first .. c_last
     const int total_tiles = a.header[kHdrTotalTiles];
     const int64_t work = (int64_t)(a.hkv / a.hg) * total_tiles;
-    int c_first = 0, c_last = -1;
-    if (si.tiles > 0) {
-        const int64_t x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
-        c_first = cta_of_tile(x0, work, a.num_ctas);
-        c_last = cta_of_tile(x0 + si.tiles - 1, work, a.num_ctas);
-    }
+    const int64_t x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
+    const int c_first = cta_of_tile(x0, work, a.num_ctas);
+    const int c_last = cta_of_tile(x0 + si.tiles - 1, work, a.num_ctas);
     const int64_t slot0 = partial_slot(a, g, b, 0);   // slot of CTA c is slot0 + c
-
-    // ---- independent loads first: the first 32 segments' lse (lane c), the
-    // draft keys' page-table entries (lane k), the query row
+    const bool all_busy = work >= a.num_ctas;          // then every CTA got at least one tile
     auto live = [&](int c) {   // CTA c covered some tile (more CTAs than tiles leaves some idle)
-        return c <= c_last && cta_start(c + 1, work, a.num_ctas) != cta_start(c, work, a.num_ctas);
+        return c <= c_last &&
+               (all_busy || cta_start(c + 1, work, a.num_ctas) != cta_start(c, work, a.num_ctas));
     };
-    float lse_mine = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * a.rows_cap + r]
-                                          : -INFINITY;
-    const int kmin = a.window >= 0 ? (i - a.window > 0 ? i - a.window : 0) : 0;
-    const int nkeys = i - kmin + 1;   // <= max_draft <= 32
-    const int indptr = __ldg(a.kv_indptr + b);
-    int64_t row_mine = -1;            // physical (slot, head) row of draft key kmin + lane
-    if (lane < nkeys) {
-        const int64_t slot = token_slot(a, indptr, (int64_t)si.prefix + kmin + lane);
-        if (slot >= 0) row_mine = slot * a.hkv + g;
-        else set_error(a, VA_ERR_BAD_PAGE);
-    }
-    const T* qg = reinterpret_cast<const T*>(a.q) + qrow * dqk;
-    const T* kc = reinterpret_cast<const T*>(a.k_cache);
-    const T* vc = reinterpret_cast<const T*>(a.v_cache);
-    float qv[kMaxQk / 32];
-#pragma unroll
-    for (int e = 0; e < kMaxQk / 32; ++e) qv[e] = (lane + 32 * e < dqk) ? to_f32(qg[lane + 32 * e]) : 0.f;
 
-    // ---- draft scores, four keys' rows in flight at a time (lane k keeps s_k)
-    float s_mine = -INFINITY;
-    for (int k0 = 0; k0 < nkeys; k0 += 4) {
-        float part[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            part[u] = 0.f;
-            const int64_t row = __shfl_sync(0xffffffffu, row_mine, (k0 + u) & 31);
-            if (k0 + u < nkeys && row >= 0) {
-                const T* kr = kc + row * a.k_row_stride;
-#pragma unroll
-                for (int e = 0; e < kMaxQk / 32; ++e)
-                    if (lane + 32 * e < dqk) part[u] = fmaf(qv[e], to_f32(kr[lane + 32 * e]), part[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
-            if (lane == k0 + u && k0 + u < nkeys) s_mine = part[u] * a.scale_log2;
-        }
-    }
-
-    // ---- M: the largest term
-    float mx = fmaxf(s_mine, lse_mine);
+    // ---- M: the largest partial lse
+    const float lse_first = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * a.rows_cap + r]
+                                                 : -INFINITY;
+    float mx = lse_first;
     for (int c = c_first + 32 + lane; c <= c_last; c += 32)
         if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * a.rows_cap + r]);
 #pragma unroll
@@ -157,7 +104,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
         const int c = cb + lane;
         float w = 0.f;
         if (live(c)) {
-            const float lc = cb == c_first ? lse_mine : a.part_lse[(slot0 + c) * a.rows_cap + r];
+            const float lc = cb == c_first ? lse_first : a.part_lse[(slot0 + c) * a.rows_cap + r];
             w = lc == -INFINITY ? 0.f : exp2f(lc - mx);
         }
         z += w;
@@ -166,7 +113,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
             float v[4][VPL], wj[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                wj[u] = __shfl_sync(0xffffffffu, w, j + u);
+                wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
                 if (j + u < n && wj[u] != 0.f)
                     load_f32<VPL>(a.part_o + ((slot0 + cb + j + u) * a.rows_cap + r) * (VPL * 32) +
                                       lane * VPL, v[u]);
@@ -178,17 +125,6 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
                     for (int e = 0; e < VPL; ++e) acc[e] = fmaf(wj[u], v[u][e], acc[e]);
                 }
         }
-    }
-    // draft keys
-    for (int k = 0; k < nkeys; ++k) {
-        const float sk = __shfl_sync(0xffffffffu, s_mine, k);
-        const int64_t vr = __shfl_sync(0xffffffffu, row_mine, k);
-        const float w = exp2f(sk - mx);
-        if (lane == 0) z += w;
-        if (vr < 0) continue;
-        const T* vp = vc + vr * a.v_row_stride + lane * VPL;
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) acc[e] = fmaf(w, to_f32(vp[e]), acc[e]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -217,8 +153,8 @@ cudaError_t launch_dtype(const Args& a, cudaStream_t s) {
 
 }  // namespace
 
-bool combine_supported(int qk_dim, int v_dim) {
-    return qk_dim <= kMaxQk && (v_dim == 64 || v_dim == 128 || v_dim == 256 || v_dim == 512);
+bool combine_supported(int, int v_dim) {
+    return v_dim == 64 || v_dim == 128 || v_dim == 256 || v_dim == 512;
 }
 
 cudaError_t launch_combine(const Args& a, int dtype, cudaStream_t s) {

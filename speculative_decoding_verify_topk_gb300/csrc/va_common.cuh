@@ -5,8 +5,10 @@
 // programs, merge the partials by log-sum-exp, handle the causal draft x draft
 // block in the combine):
 //
-//   * The prefix of sequence b that any of its rows can see is [lo_b, P_b),
-//     lo_b = max(0, P_b - window) (row 0 has the lowest window bound). It is
+//   * The keys any row of sequence b can see are [lo_b, P_b + D_b): the
+//     prefix from lo_b = max(0, P_b - window) (row 0 has the lowest window
+//     bound) plus the drafts, which the last tile carries with a per-row
+//     causal bound (row i sees keys up to P_b + i). The range is
 //     cut into TT-token tiles aligned to absolute positions (TT = the plan's
 //     tile_tokens, 64 or 128): tile t covers [a_b + TT t, a_b + TT (t + 1)),
 //     a_b = lo_b rounded down to a multiple of TT.
@@ -42,10 +44,10 @@ enum HeaderWord { kHdrError = 0, kHdrTotalTiles = 1, kHdrBs = 2 };
 struct SeqInfo {
     int32_t qoff;      // first query row of the sequence: sum_{b' < b} D_b'
     int32_t prefix;    // P_b
-    int32_t draft;     // D_b (0 when the sequence failed a check)
-    int32_t lo;        // lowest prefix key any row sees: max(0, P_b - window)
+    int32_t draft;     // D_b (capped at max_draft)
+    int32_t lo;        // lowest key any row sees: max(0, P_b - window)
     int32_t a0;        // first tile start: lo rounded down to a multiple of the tile
-    int32_t tiles;     // prefix tiles
+    int32_t tiles;     // tiles over [a0, P_b + D_b)
     int32_t tile_off;  // exclusive prefix sum of tiles
     int32_t bad;       // nonzero: the sequence failed a device check; its rows are NaN
 };

@@ -2,8 +2,9 @@
 //
 // Same work decomposition and partial-result contract as the bf16 / fp16
 // kernel (see va_common.cuh): each persistent CTA walks its share of the tile
-// stream and writes one normalised partial output plus its base-2
-// log-sum-exp per segment. fp32 inputs keep the 1e-4 accuracy bar, so the
+// stream (the prefix and, in each sequence's last tile, the causal drafts)
+// and writes one normalised partial output plus its base-2 log-sum-exp per
+// segment. fp32 inputs keep the 1e-4 accuracy bar, so the
 // contractions run on the CUDA cores in fp32: warp w owns query rows
 // w, w + 4, ...; lanes own tokens for Q.K and output columns for P.V. Each
 // 64-token K/V tile is gathered with 16-byte cp.async into padded shared
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
         if (tid < kTile) {
             const int64_t j = (int64_t)j0 + tid;
             int64_t row = -1;
-            if (j >= si.lo && j < si.prefix) {
+            if (j >= si.lo && j < si.prefix + si.draft) {
                 const int64_t slot = token_slot(a, __ldg(a.kv_indptr + cur.b), j);
                 if (slot >= 0) row = slot * a.hkv + cur.g;
                 else set_error(a, VA_ERR_BAD_PAGE);
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
         for (int r = warp; r < rows_b; r += kWarps) {
             const int i = r / a.group;
             const int lo_r = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
+            const int hi_r = si.prefix + i;   // causal: drafts 0 .. i
             float sc[2];
             for (int h = 0; h < 2; ++h) {
                 const int t = lane + 32 * h;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
                     acc = fmaf(x.z, y.z, acc);
                     acc = fmaf(x.w, y.w, acc);
                 }
-                sc[h] = (j >= si.prefix || j < lo_r || j < si.lo) ? -INFINITY : acc * a.scale_log2;
+                sc[h] = (j > hi_r || j < lo_r || j < si.lo) ? -INFINITY : acc * a.scale_log2;
             }
             float mx = fmaxf(sc[0], sc[1]);
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));

@@ -7,8 +7,8 @@
 // sequence b, a run of prefix keys -- the normalised partial attention output
 // of the G * D_b query rows of every kv-head g in the group, and its base-2
 // log-sum-exp. Rows of head g are r = i * G + hh (draft i, q-head g * G + hh);
-// row r's window lower bound is P_b + i - window. Keys j >= P_b (the drafts)
-// are left to the combine kernel.
+// row r sees keys j with P_b + i - window <= j <= P_b + i: the prefix and,
+// in the sequence's last tile, the causal draft x draft block.
 //
 // GB300 mapping. The path is HBM-bound (16-40 flop per KV byte):
 //   * A tile is TT = 16 tokens of one sequence for all HG heads of the group.
@@ -30,9 +30,9 @@
 //     results need no cross-warp merge; each warp releases the stage with one
 //     arrive. Query fragments are read straight from global memory at the
 //     start of a segment (a few per CTA).
-//   * V rows of tokens at or past P_b may hold another sequence's data or
-//     garbage; in the tiles that reach P_b each consumer zeroes its head's V
-//     rows there before P V (0 * NaN would poison the sum).
+//   * V rows of tokens at or past P_b + D_b may hold another sequence's data
+//     or garbage; in the tiles that reach that far each consumer zeroes its
+//     head's V rows there before P V (0 * NaN would poison the sum).
 // Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT
 // and the CTA winds down (no further waits) instead of hanging.
 #pragma once
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Lane c < ppt owns page chunk c of a tile. Its page-table read for
         // tile k + 2 is issued in iteration k and used in iteration k + 1.
         Cursor ahead = cur;
-        int cached_b = -1, s_a0 = 0, s_lo = 0, s_prefix = 0, s_indptr = 0;
+        int cached_b = -1, s_a0 = 0, s_lo = 0, s_end = 0, s_indptr = 0;
         int p_page = -1, p_off = 0;         // pending (tile k + 1): page id, first slot offset
         bool p_valid = false;
         int n_page = -1, n_off = 0;         // tile being issued (k)
@@ -161,12 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto start = [&]() {
             if (ahead.b != cached_b) {
                 const SeqInfo si = a.seq[ahead.b];
-                s_a0 = si.a0; s_lo = si.lo; s_prefix = si.prefix;
+                s_a0 = si.a0; s_lo = si.lo; s_end = si.prefix + si.draft;
                 s_indptr = __ldg(a.kv_indptr + ahead.b);
                 cached_b = ahead.b;
             }
             const int jc = s_a0 + ahead.t * kTT + lane * geo.tb;   // first token of chunk `lane`
-            p_valid = lane < geo.ppt && jc < s_prefix && jc + geo.tb > s_lo;
+            p_valid = lane < geo.ppt && jc < s_end && jc + geo.tb > s_lo;
             p_off = jc % a.page_size;
             p_page = p_valid ? __ldg(a.page_table + s_indptr + jc / a.page_size) : -1;
         };
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qf[DQK / 16][4];
         float o[DV / 8][4];
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-        int rows_b = 0, lo_r[2] = {0, 0};
+        int rows_b = 0, lo_r[2] = {0, 0}, hi_r[2] = {0, 0};
         SeqInfo si = {};
         auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
             if (*(volatile int*)&abort_flag) return;
@@ -281,9 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run[0] = m_run[1] = -INFINITY;
                 l_run[0] = l_run[1] = 0.f;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i = (wm * 16 + (lane >> 2) + 8 * h) / a.group;
+                for (int h = 0; h < 2; ++h) {   // row i sees keys [P + i - window, P + i]
+                    const int r = wm * 16 + (lane >> 2) + 8 * h;
+                    const int i = r / a.group;
                     lo_r[h] = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
+                    hi_r[h] = r < rows_b ? si.prefix + i : -0x7fffffff;   // padding rows see nothing
                 }
             }
             wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
@@ -292,13 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
             const int tile_j0 = si.a0 + cur.t * kTT;
 
-            // V rows of tokens at or past the prefix end: zero them (this head)
-            const bool tail = tile_j0 + kTT > si.prefix;
+            // V rows of tokens past the sequence's end: zero them (this head)
+            const int seq_end = si.prefix + si.draft;
+            const bool tail = tile_j0 + kTT > seq_end;
             if (tail) {
                 for (int idx = lane; idx < kTT * geo.nhv * 8; idx += 32) {
                     const int t = idx / (geo.nhv * 8), rem = idx - t * geo.nhv * 8;
                     const int h = rem >> 3, ch = rem & 7;
-                    if (tile_j0 + t >= si.prefix)
+                    if (tile_j0 + t >= seq_end)
                         *reinterpret_cast<uint4*>(stage + (geo.nhk + h) * geo.half_bytes + rowaddr(t, ch)) =
                             make_uint4(0, 0, 0, 0);
                 }
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ---- scale, mask, online softmax (rows lane/4 and lane/4 + 8 of the m-tile)
-            const bool need_mask = tail ||
+            const bool need_mask = tile_j0 + kTT > si.prefix ||
                                    (a.window >= 0 && tile_j0 < si.prefix + si.draft - 1 - a.window);
             const int j_base = tile_j0 + 2 * (lane & 3);
             float mx[2] = {-INFINITY, -INFINITY};
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v = s[n][e] * a.scale_log2;
                     if (need_mask) {
                         const int j = j_base + n * 8 + (e & 1);
-                        if (j >= si.prefix || j < lo_r[e >> 1]) v = -INFINITY;
+                        if (j > hi_r[e >> 1] || j < lo_r[e >> 1]) v = -INFINITY;
                     }
                     s[n][e] = v;
                     mx[e >> 1] = fmaxf(mx[e >> 1], v);

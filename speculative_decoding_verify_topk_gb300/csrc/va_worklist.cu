@@ -1,8 +1,8 @@
 // Work-list kernel: per-sequence facts for the prefix and combine kernels.
 //
 // One CTA of 1024 threads. For every sequence it checks the lengths and the
-// page-table capacity, derives the prefix range any row can see (the window's
-// lowest bound belongs to row 0), counts the 64-token prefix tiles, and takes
+// page-table capacity, derives the key range any row can see, [lo, P + D)
+// (the window's lowest bound belongs to row 0), counts its tiles, and takes
 // two exclusive prefix sums: query rows (qoff) and tiles (tile_off). The grid
 // of the later kernels depends only on host-known sizes; everything that
 // depends on tensor values is computed here, on the device, so a call can be
@@ -74,10 +74,11 @@ __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
             qrows = d > 0 ? d : 0;
             si.draft = qrows < a.max_draft ? qrows : a.max_draft;
             if (!bad && qrows > 0) {
+                // keys any row sees: [lo, P + D); row i's window starts at P + i - window
                 const int lo = (a.window >= 0 && p - a.window > 0) ? p - a.window : 0;
                 si.lo = lo;
                 si.a0 = lo - lo % a.tile;
-                tiles = p > lo ? (p - si.a0 + a.tile - 1) / a.tile : 0;
+                tiles = (p + qrows - si.a0 + a.tile - 1) / a.tile;
             }
             si.tiles = tiles;
         }
