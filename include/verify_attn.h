@@ -193,6 +193,13 @@ const char *verify_attn_status_string(int status);
 int verify_attn_check(const va_plan *plan, const void *workspace, void *stream,
                       int32_t *error_bits);
 
+/*
+ * Text describing the most recent VA_CUDA_ERROR returned on the calling
+ * thread: which step failed and the CUDA runtime's message ("" if none).
+ * Thread-local, valid until the thread's next call into the library.
+ */
+const char *verify_attn_last_error(void);
+
 /* Number of kernel launches one verify_attn_paged call makes for this plan. */
 int verify_attn_launches_per_call(const va_plan *plan);
 

@@ -20,7 +20,7 @@ VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
-           "verify_attn_paged_static")
+           "verify_attn_paged_static", "verify_attn_last_error")
 
 
 class Problem(ctypes.Structure):
@@ -49,7 +49,10 @@ class Plan(ctypes.Structure):
 class VerifyAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        detail = ""
+        if status == VA_CUDA_ERROR:
+            detail = " -- " + load_library().verify_attn_last_error().decode()
+        super().__init__(f"{what}: {status_string(status)} (status {status}){detail}")
 
 
 _lib = None
@@ -81,6 +84,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.verify_attn_status_string.restype = ctypes.c_char_p
         lib.verify_attn_check.argtypes = [ctypes.POINTER(Plan), P, P, ctypes.POINTER(ctypes.c_int32)]
         lib.verify_attn_check.restype = I
+        lib.verify_attn_last_error.argtypes = []
+        lib.verify_attn_last_error.restype = ctypes.c_char_p
         lib.verify_attn_launches_per_call.argtypes = [ctypes.POINTER(Plan)]
         lib.verify_attn_launches_per_call.restype = I
         _lib = lib

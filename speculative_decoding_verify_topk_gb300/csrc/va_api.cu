@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 
 #include "va_common.cuh"
@@ -88,6 +89,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool is_aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+thread_local char g_last_error[256];
+
+// Records what failed for verify_attn_last_error() and returns VA_CUDA_ERROR.
+int cuda_failure(const char* step, cudaError_t e) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", step, cudaGetErrorString(e), (int)e);
+    cudaGetLastError();   // clear a non-sticky error so the next call starts clean
+    return VA_CUDA_ERROR;
+}
+
 }  // namespace
 
 extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
@@ -118,9 +128,14 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.path = VA_PATH_F32;
         ctas_per_sm = smem <= 100 * 1024 ? 2 : 1;
         out.tile_tokens = va::kTile;
-    } else if (p.v_aliases_k && p.num_kv_heads == 1 && p.qk_dim == 576 && p.v_dim == 512 &&
-               p.dtype == VA_BF16 && va::mla_available() && out.rows_cap <= 1024) {
+    } else if (p.v_aliases_k && p.num_kv_heads == 1 && p.num_q_heads == 128 && p.qk_dim == 576 &&
+               p.v_dim == 512 && p.dtype == VA_BF16 && va::mla_available() &&
+               va::mla_page_size_ok(p.page_size)) {
+        // absorbed MLA: 64-token tiles, one 2-CTA cluster per 128-row block
         out.path = VA_PATH_MLA;
+        out.tile_tokens = 64;
+        out.heads_per_cta = 1;
+        out.stages = va::mla_stages();
         ctas_per_sm = 1;
     } else {
         // bf16 / fp16: a CTA takes hg kv-heads (the largest divisor of Hkv with
@@ -158,7 +173,17 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         }
     }
     out.num_ctas = p.num_ctas > 0 ? p.num_ctas : sms * ctas_per_sm;
-    const int64_t slots = (int64_t)p.num_kv_heads * p.max_bs + (int64_t)out.heads_per_cta * out.num_ctas;
+    int64_t slots, slot_rows;
+    if (out.path == VA_PATH_MLA) {
+        out.num_ctas &= ~1;   // whole clusters of two
+        if (out.num_ctas < 2) return VA_INVALID_ARG;
+        // (row block = draft, sequence, cluster) slots of 128 rows
+        slots = (int64_t)p.max_draft * (p.max_bs + out.num_ctas / 2);
+        slot_rows = 128;
+    } else {
+        slots = (int64_t)p.num_kv_heads * p.max_bs + (int64_t)out.heads_per_cta * out.num_ctas;
+        slot_rows = out.rows_cap;
+    }
     if (slots > INT32_MAX) return VA_UNSUPPORTED;
     out.num_slots = (int)slots;
 
@@ -166,9 +191,9 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     out.off_seq = off;
     off = align_up(off + sizeof(va::SeqInfo) * (size_t)p.max_bs);
     out.off_part_lse = off;
-    off = align_up(off + sizeof(float) * (size_t)slots * out.rows_cap);
+    off = align_up(off + sizeof(float) * (size_t)slots * slot_rows);
     out.off_part_o = off;
-    off = align_up(off + sizeof(float) * (size_t)slots * out.rows_cap * p.v_dim);
+    off = align_up(off + sizeof(float) * (size_t)slots * slot_rows * p.v_dim);
     out.workspace_bytes = off;
     *plan = out;
     return VA_OK;
@@ -232,6 +257,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.num_ctas = plan->num_ctas;
     a.tile = plan->tile_tokens;
     a.hg = plan->heads_per_cta;
+    a.mla = plan->path == VA_PATH_MLA;
     if (a.hg < 1 || p.num_kv_heads % a.hg != 0) return VA_INVALID_ARG;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -241,9 +267,10 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
     };
     cudaError_t e;
+    g_last_error[0] = '\0';
     rec(0);
     e = va::launch_worklist(a, s);
-    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (e != cudaSuccess) return cuda_failure("work-list launch", e);
     rec(1);
     switch (plan->path) {
     case VA_PATH_F32: e = va::launch_prefix_f32(a, s); break;
@@ -272,14 +299,14 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
                                  p.num_kv_heads, g.tb, g.hg) ||
             !va::encode_pool_map(&vmap, a.v_cache, p.dtype, p.v_dim, (int)a.v_row_stride, slots,
                                  p.num_kv_heads, g.tb, g.hg))
-            return VA_CUDA_ERROR;
+            return cuda_failure("tensor-map encoding", cudaErrorInvalidValue);
         e = fn(kmap, vmap, a, g, p.dtype, s);
     }
     }
-    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (e != cudaSuccess) return cuda_failure("prefix launch", e);
     rec(2);
     e = va::launch_combine(a, p.dtype, s);
-    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (e != cudaSuccess) return cuda_failure("combine launch", e);
     rec(3);
     return VA_OK;
 }
@@ -330,6 +357,8 @@ extern "C" int verify_attn_check(const va_plan* plan, const void* workspace, voi
     if (error_bits) *error_bits = word;
     return word ? VA_DEVICE_RANGE_ERROR : VA_OK;
 }
+
+extern "C" const char* verify_attn_last_error(void) { return g_last_error; }
 
 extern "C" int verify_attn_launches_per_call(const va_plan* plan) {
     return plan ? 3 : 0;

@@ -73,25 +73,42 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
         return;
     }
 
-    // ---- the segments that covered (g, b): CTAs c_first .. c_last
+    // ---- the segments that covered this row: workers c_first .. c_last of the
+    // partition. GQA: the stream is over (head group, sequence, tile) and the
+    // workers are CTAs; MLA: over (row block = draft, sequence, tile) and the
+    // workers are 2-CTA clusters, whose slots hold 128 rows.
     const int total_tiles = a.header[kHdrTotalTiles];
-    const int64_t work = (int64_t)(a.hkv / a.hg) * total_tiles;
-    const int64_t x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
-    const int c_first = cta_of_tile(x0, work, a.num_ctas);
-    const int c_last = cta_of_tile(x0 + si.tiles - 1, work, a.num_ctas);
-    const int64_t slot0 = partial_slot(a, g, b, 0);   // slot of CTA c is slot0 + c
-    const bool all_busy = work >= a.num_ctas;          // then every CTA got at least one tile
-    auto live = [&](int c) {   // CTA c covered some tile (more CTAs than tiles leaves some idle)
+    int64_t work, x0, slot0, slot_rows, prow;
+    int workers;
+    if (a.mla) {
+        workers = a.num_ctas / 2;
+        work = (int64_t)a.max_draft * total_tiles;
+        x0 = (int64_t)i * total_tiles + si.tile_off;
+        slot0 = (int64_t)i * (a.bs + workers) + b;
+        slot_rows = 128;
+        prow = h;
+    } else {
+        workers = a.num_ctas;
+        work = (int64_t)(a.hkv / a.hg) * total_tiles;
+        x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
+        slot0 = partial_slot(a, g, b, 0);   // slot of CTA c is slot0 + c
+        slot_rows = a.rows_cap;
+        prow = r;
+    }
+    const int c_first = cta_of_tile(x0, work, workers);
+    const int c_last = cta_of_tile(x0 + si.tiles - 1, work, workers);
+    const bool all_busy = work >= workers;   // then every worker got at least one tile
+    auto live = [&](int c) {   // worker c covered some tile (more workers than tiles leaves some idle)
         return c <= c_last &&
-               (all_busy || cta_start(c + 1, work, a.num_ctas) != cta_start(c, work, a.num_ctas));
+               (all_busy || cta_start(c + 1, work, workers) != cta_start(c, work, workers));
     };
 
     // ---- M: the largest partial lse
-    const float lse_first = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * a.rows_cap + r]
+    const float lse_first = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * slot_rows + prow]
                                                  : -INFINITY;
     float mx = lse_first;
     for (int c = c_first + 32 + lane; c <= c_last; c += 32)
-        if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * a.rows_cap + r]);
+        if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * slot_rows + prow]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
@@ -104,7 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
         const int c = cb + lane;
         float w = 0.f;
         if (live(c)) {
-            const float lc = cb == c_first ? lse_first : a.part_lse[(slot0 + c) * a.rows_cap + r];
+            const float lc = cb == c_first ? lse_first : a.part_lse[(slot0 + c) * slot_rows + prow];
             w = lc == -INFINITY ? 0.f : exp2f(lc - mx);
         }
         z += w;
@@ -115,7 +132,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
             for (int u = 0; u < 4; ++u) {
                 wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
                 if (j + u < n && wj[u] != 0.f)
-                    load_f32<VPL>(a.part_o + ((slot0 + cb + j + u) * a.rows_cap + r) * (VPL * 32) +
+                    load_f32<VPL>(a.part_o + ((slot0 + cb + j + u) * slot_rows + prow) * (VPL * 32) +
                                       lane * VPL, v[u]);
             }
 #pragma unroll

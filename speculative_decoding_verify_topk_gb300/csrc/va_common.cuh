@@ -38,7 +38,7 @@ constexpr int kMaxDraft = 32;      // largest supported num_draft (one lane per 
 constexpr int kHeaderBytes = 256;  // workspace header: error word, totals
 
 // Header words (int32) at the start of the workspace.
-enum HeaderWord { kHdrError = 0, kHdrTotalTiles = 1, kHdrBs = 2 };
+enum HeaderWord { kHdrError = 0, kHdrTotalTiles = 1, kHdrBs = 2, kHdrWaitSites = 3 };
 
 // Per-sequence facts computed by the work-list kernel (32 bytes).
 struct SeqInfo {
@@ -75,6 +75,8 @@ struct Args {
     int num_ctas;            // persistent CTAs of the prefix kernel
     int tile;                // KV tokens per prefix tile (the plan's tile_tokens)
     int hg;                  // kv-heads a prefix CTA handles together (1 on the fp32 path)
+    int mla;                 // 1: absorbed-MLA layout (row blocks of 128 heads per draft,
+                             //    2-CTA clusters, partial slots of 128 rows)
     float scale_log2;        // scale * log2(e)
     float scale;
 };
@@ -124,6 +126,8 @@ cudaError_t launch_prefix_mla(const Args& a, cudaStream_t s);
 cudaError_t launch_combine(const Args& a, int dtype, cudaStream_t s);
 size_t prefix_f32_smem_bytes(int qk_dim, int v_dim, int rows_cap);
 bool combine_supported(int qk_dim, int v_dim);
+int mla_stages();
+bool mla_page_size_ok(int page_size);
 bool prefix_mma_built(int qk_dim, int v_dim);
 
 // ---------------------------------------------------------------------------

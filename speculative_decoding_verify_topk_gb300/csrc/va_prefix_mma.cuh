@@ -122,6 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Rows a tile never fills (boxes wholly outside the visible keys) must not
+    // hold NaN bit patterns on a stage's first use: zero the ring once.
+    for (int i = tid; i < geo.stages * geo.stage_bytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (tid == 0) {
         for (int s = 0; s < geo.stages; ++s) {
             mbar_init(bar_full + 8 * s, 1);

@@ -47,7 +47,10 @@ __device__ int block_exclusive_scan(int v, int* excl, int* warp_sums) {
 __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
     __shared__ int warp_sums[33];
     pdl_launch_dependents();   // the prefix kernel may start its set-up now
-    if (threadIdx.x == 0) a.header[kHdrError] = 0;
+    if (threadIdx.x == 0) {
+        a.header[kHdrError] = 0;
+        a.header[kHdrWaitSites] = 0;
+    }
     __syncthreads();
 
     int q_carry = 0, tile_carry = 0, err = 0;

@@ -239,3 +239,65 @@ def test_cuda_graph_replay_with_new_lengths():
         assert_close("graph out", out[: p.total_q].double().cpu().numpy(), ref_o, atol, rtol)
         assert_close("graph lse", lse[: p.total_q].double().cpu().numpy(), ref_l, latol, 0)
     assert attn.check() == 0
+
+
+# ---------------------------------------------------------------------------
+# absorbed MLA (tcgen05 / TMEM kernel, 2-CTA clusters)
+# ---------------------------------------------------------------------------
+
+def test_mla_plan_selects_tensor_core_path():
+    pb = synth.make_batch(small("dsv3_mla")).to("cuda")
+    wl = pb.wl
+    attn = va.VerifyAttention(max_bs=wl.bs, max_draft=3, num_q_heads=128, num_kv_heads=1,
+                              qk_dim=576, v_dim=512, page_size=pb.page_size, dtype=wl.dtype,
+                              max_kv_len=4096, num_pages=pb.num_pages, v_aliases_k=True)
+    assert attn.plan.path == va.VA_PATH_MLA and attn.plan.tile_tokens == 64
+    assert attn.plan.num_ctas % 2 == 0
+
+
+@pytest.mark.parametrize("window", [-1, 0, 2, 100])
+def test_mla_small(window):
+    check(synth.make_batch(small("dsv3_mla")), window=window)
+
+
+@pytest.mark.parametrize("num_ctas", [2, 6, 40])
+def test_mla_partition_invariance(num_ctas):
+    check(synth.make_batch(small("dsv3_mla")), num_ctas=num_ctas)
+
+
+def test_mla_page_sizes_and_ragged_drafts():
+    """Page sizes 16 and 64 (boxes of 16 and 64 tokens), empty prefixes, and
+    sequences with fewer drafts than the plan's row blocks."""
+    wl = small("dsv3_mla", bs=4)
+    lg = synth.make_logical(wl, seq_lens=[0, 63, 64, 500], num_draft=[3, 1, 2, 3])
+    for ps, seed in ((16, 3), (64, 4)):
+        check(synth.paginate(lg, page_size=ps, seed=seed), max_draft=3)
+
+
+def test_mla_long_prefix():
+    """Several thousand keys per sequence: many tiles per cluster, segments
+    spanning clusters, and the lazy O rescale in tensor memory."""
+    check(synth.make_batch(small("dsv3_mla", bs=2, prefix=("uniform", 3000, 6000))))
+
+
+def test_mla_growing_scores_force_rescales():
+    """Keys scaled up along the sequence so the running max jumps by more than
+    2^8 many times: every row block rescales O in tensor memory repeatedly,
+    rows of one warp at different tiles."""
+    wl = small("dsv3_mla", bs=2, prefix=("uniform", 1500, 2500))
+    lg = synth.make_logical(wl)
+    for b in range(wl.bs):
+        t0, t1 = int(lg.tok_off[b]), int(lg.tok_off[b + 1])
+        ramp = torch.linspace(0.2, 3.0, t1 - t0).view(-1, 1, 1)
+        lg.k[t0:t1] = (lg.k[t0:t1].float() * ramp).to(lg.k.dtype)
+    check(synth.paginate(lg))
+
+
+def test_gqa_growing_scores():
+    wl = small("llama8b_gqa", bs=2, prefix=("uniform", 1500, 2500))
+    lg = synth.make_logical(wl)
+    for b in range(wl.bs):
+        t0, t1 = int(lg.tok_off[b]), int(lg.tok_off[b + 1])
+        ramp = torch.linspace(0.2, 3.0, t1 - t0).view(-1, 1, 1)
+        lg.k[t0:t1] = (lg.k[t0:t1].float() * ramp).to(lg.k.dtype)
+    check(synth.paginate(lg))
