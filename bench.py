@@ -460,6 +460,8 @@ def ours_arm(args):
         tf = acct["flops"] / (prefix_avg_ms * 1e-3) / 1e12
         roofline.update({"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]),
                          "unit": "TFLOP/s", "frac": tf / float(peaks["bf16_tflops"]),
+                         "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json, burst)"
+                         if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
                          "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak})
     cpu = None
     if not args.no_cpu_baseline:

@@ -177,6 +177,10 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     if (out.path == VA_PATH_MLA) {
         out.num_ctas &= ~1;   // whole clusters of two
         if (out.num_ctas < 2) return VA_INVALID_ARG;
+        // by default a multiple of max_draft clusters, so that the row blocks'
+        // clusters stream the same KV tiles at the same time (L2 reuse)
+        const int pairs = out.num_ctas / 2;
+        if (p.num_ctas == 0 && pairs >= p.max_draft) out.num_ctas = 2 * (pairs - pairs % p.max_draft);
         // (row block = draft, sequence, cluster) slots of 128 rows
         slots = (int64_t)p.max_draft * (p.max_bs + out.num_ctas / 2);
         slot_rows = 128;

@@ -12,28 +12,37 @@
 // Why this shape: 128 heads x D drafts make 128-row blocks of a real dense
 // contraction (~725 flop per KV byte), so it runs on tcgen05.mma with fp32
 // accumulators in tensor memory (TMEM). A 128-row block's output for v_dim 512
-// fills all 512 TMEM columns, leaving no room for the scores. So a cluster of
-// two CTAs (ranks 0 and 1) shares one row block:
-//   * the QK^T contraction over 576 columns is split: rank 0 takes columns
-//     0..255, rank 1 256..575; each holds only its slice of Q and of every KV
-//     tile in shared memory;
-//   * each rank writes its partial score tile (128 x 64 fp32) into the other
-//     rank's shared memory (distributed shared memory) and adds the other's:
-//     both then hold identical scores and run the identical online softmax;
-//   * each rank accumulates O for its half of v_dim (rank r: columns
-//     256 r .. 256 r + 255, which lie inside the KV slice it loaded) with
-//     P from shared memory: O (128 x 256 fp32) in TMEM columns 256..511, the
-//     double-buffered partial scores in columns 0..127.
-// Roles per CTA: warp 0 issues TMA (KV tile slices, query slices), warp 1 issues
-// the MMAs (one thread) and commits them to mbarriers, warps 2..5 (128
-// threads, thread = row) read scores from TMEM, exchange them, run the
-// softmax, write P, rescale O in TMEM when the running max moves by more than
+// would fill all 512 TMEM columns, so a cluster of two CTAs (ranks 0 and 1)
+// shares one row block:
+//   * both ranks compute the full score tile S = Q K^T (128 rows x 64 tokens,
+//     576 columns) and run the identical online softmax on it. Exchanging
+//     partial scores between the two SMs through distributed shared memory
+//     measured slower than computing them twice;
+//   * rank r accumulates O for v columns 256 r .. 256 r + 255 (128 x 256 fp32
+//     in TMEM columns 256..511); the scores use columns 0..63;
+//   * the query row block is the A operand of the score MMAs: its first six
+//     64-column chunks sit in TMEM columns 64..255 (an MMA reading A from TMEM
+//     issues faster than one reading it from shared memory), the last three in
+//     shared memory;
+//   * every KV tile and the shared-memory query chunks are fetched once for
+//     the pair: each rank issues half of the TMA boxes with cluster
+//     multicast, and a stage is refilled only after both ranks' MMAs have
+//     released it (MMA completion multicast to both).
+// Roles per CTA: warp 0 issues TMA; warp 1 issues the MMAs (one thread,
+// event-driven: P V of a tile as soon as its P is written, the scores of the
+// next tile as soon as its stage has landed, so they overlap the softmax);
+// warps 2..5 (128 threads, thread = row) write the TMEM part of the query at
+// a segment start, read scores from TMEM, run the softmax, write P (bf16) to
+// shared memory, rescale O in TMEM when the running max moves by more than
 // 2^8 (lazy rescaling), and write the segment's normalised partial output.
 //
 // Work decomposition: tiles of 64 tokens; the stream runs over (row block =
 // draft i, sequence b, tile), and the persistent grid's clusters take equal
-// contiguous shares of it, exactly as the GQA kernels' CTAs do. Every wait is
-// bounded (VA_ERR_TIMEOUT, then the kernel winds down without waiting).
+// contiguous shares of it, exactly as the GQA kernels' CTAs do. With the
+// cluster count a multiple of the draft count, the clusters of different row
+// blocks walk the same KV tiles at the same time, so a tile read from HBM for
+// one row block is served from L2 for the others. Every wait is bounded
+// (VA_ERR_TIMEOUT, then the kernel winds down without waiting).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -47,11 +56,18 @@ constexpr int kTok = 64;          // tokens per tile (N of the score MMA, K of t
 constexpr int kRows = 128;        // rows per block (M of both MMAs)
 constexpr int kQk = 576, kV = 512;
 constexpr int kChunk = 64;        // columns per 128-byte swizzle chunk
+constexpr int kChunks = kQk / kChunk;   // 9
+constexpr int kQTmem = 6;         // query chunks 0..5 in TMEM (32 columns each), 6..8 in shared memory
 constexpr int kThreads = 192;     // producer, MMA, 4 softmax warps
-constexpr int kXStride = kTok * 4 + 16;   // padded exchange row (bytes)
+constexpr int kQBytes = (kChunks - kQTmem) * kRows * 128;   // [chunk][128 rows][128 B], 128-byte swizzle
+constexpr int kStageBytes = kChunks * kTok * 128;           // [chunk][64 tokens][128 B], 128-byte swizzle
+constexpr int kPBytes = kRows * kTok * 2;                   // P: [128 rows][128 B], 128-byte swizzle
+constexpr uint32_t kColS = 0, kColQ = 64, kColO = 256;      // TMEM columns
+// the MMA issuer's no-progress limit in SM cycles (about 2 s at 2 GHz, longer at lower clocks)
+constexpr long long kSpinCycles = 1LL << 32;
 
 struct MlaGeo {
-    int stages;          // KV ring depth (per rank)
+    int stages;          // KV ring depth
     int tb;              // tokens per TMA box: gcd(page_size, 64)
     int pairs;           // clusters in the grid
     int smem_bytes;
@@ -65,44 +81,12 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
-__device__ __forceinline__ void arrive_peer(uint32_t peer_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(peer_bar) : "memory");
-}
-// wait with cluster-scope acquire (the phase may be completed by the peer CTA)
-__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity) {
-    if (try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (try_wait_cluster(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
 
-// tcgen05 shared-memory matrix descriptor, 128-byte swizzle
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// tcgen05 shared-memory matrix descriptor (sm_100 format: version 1 at bit 46,
+// layout type at bits 61..63: 0 = no swizzle, 2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
     return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
 }
 // instruction descriptor: bf16 x bf16 -> fp32, M x N, operand majors (0 = K, 1 = MN)
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -116,9 +100,25 @@ __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_
         "l"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
+// the same with the A operand in TMEM (rows = lanes, bf16 pairs per 32-bit column)
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+// arrive on this CTA's barrier once the MMAs issued so far have completed
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
                  : "memory");
+}
+// the same, arriving on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(bar),
+        "h"((unsigned short)3)
+        : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
@@ -144,12 +144,31 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
         "r"(r[29]), "r"(r[30]), "r"(r[31])                                                           \
         : "memory")
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+// 2-d TMA box into the same shared-memory offset of both CTAs of the pair;
+// each receiving CTA's barrier at `bar`'s offset counts the bytes
+__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-        "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar), "h"((unsigned short)3)
         : "memory");
+}
+
+// non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Partial-result slot of (row block rb, sequence b) written by cluster p.
@@ -163,66 +182,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t rank = cluster_rank();
-    const uint32_t peer = rank ^ 1u;
-    // this rank's column slice of Q and K: rank 0 -> chunks 0..3, rank 1 -> chunks 4..8.
-    // Both ranks use the same layout (sized for five chunks): distributed
-    // shared-memory addresses (the exchange buffer, the barriers) map by offset.
-    const int c_begin = rank == 0 ? 0 : 4, n_chunks = rank == 0 ? 4 : 5;
-    constexpr int kMaxChunks = 5;
-    const int q_bytes = kMaxChunks * kRows * 128;          // [chunk][128 rows][128 B]
-    const int stage_bytes = kMaxChunks * kTok * 128;       // [chunk][64 tokens][128 B]
-    unsigned char* const qs = base;
-    unsigned char* const ring = qs + q_bytes;
-    unsigned char* const ps = ring + geo.stages * stage_bytes;   // P: [128 rows][64 tokens] bf16, SW128
-    unsigned char* const xs = ps + kRows * 128;                   // peer's partial scores [128][kXStride]
-    uint64_t* const bars = reinterpret_cast<uint64_t*>(xs + kRows * kXStride);
-    const uint32_t b_kfull = smem_u32(bars);                     // [stages] tx
-    const uint32_t b_kempty = b_kfull + 8 * geo.stages;          // [stages] mma commit
-    const uint32_t b_qfull = b_kempty + 8 * geo.stages;          // tx
-    const uint32_t b_qfree = b_qfull + 8;                        // mma commit
-    const uint32_t b_sfull = b_qfree + 8;                        // [2] mma commit
-    const uint32_t b_sfree = b_sfull + 16;                       // [2] 128 softmax threads
-    const uint32_t b_pfull = b_sfree + 16;                       // 128 softmax threads
-    const uint32_t b_pvdone = b_pfull + 8;                       // mma commit
-    const uint32_t b_xfull = b_pvdone + 8;                       // 128 peer arrivals
-    const uint32_t b_xfree = b_xfull + 8;                        // 128 peer arrivals
+    // Both ranks use the same layout: multicast copies and commits address
+    // the peer's buffers and barriers by this CTA's offsets.
+    unsigned char* const qs = base;                               // query chunks 6..8
+    unsigned char* const ring = qs + kQBytes;
+    unsigned char* const ps = ring + geo.stages * kStageBytes;
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(ps + kPBytes);
+    const uint32_t b_kfull = smem_u32(bars);                     // [stages] own arrive + tx from both ranks
+    const uint32_t b_kempty = b_kfull + 8 * geo.stages;          // [stages] MMA commits of both ranks
+    const uint32_t b_qfull = b_kempty + 8 * geo.stages;          // own arrive + tx from both ranks
+    const uint32_t b_qfree = b_qfull + 8;                        // MMA commits of both ranks
+    const uint32_t b_qtmem = b_qfree + 8;                        // 128 softmax threads (TMEM query written)
+    const uint32_t b_sfull = b_qtmem + 8;                        // MMA commit
+    const uint32_t b_sfree = b_sfull + 8;                        // 128 softmax threads
+    const uint32_t b_pfull = b_sfree + 8;                        // 128 softmax threads
+    const uint32_t b_pvdone = b_pfull + 8;                       // MMA commit
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Rows a tile never fills (boxes wholly outside the visible keys, queries of
     // absent drafts) must not hold NaN bit patterns: zero Q and the ring once.
-    for (int i = tid; i < (q_bytes + geo.stages * stage_bytes) / 16; i += kThreads)
+    for (int i = tid; i < (kQBytes + geo.stages * kStageBytes) / 16; i += kThreads)
         reinterpret_cast<uint4*>(qs)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
         for (int s = 0; s < geo.stages; ++s) {
             mbar_init(b_kfull + 8 * s, 1);
-            mbar_init(b_kempty + 8 * s, 1);
+            mbar_init(b_kempty + 8 * s, 2);
         }
         mbar_init(b_qfull, 1);
-        mbar_init(b_qfree, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(b_sfull + 8 * s, 1);
-            mbar_init(b_sfree + 8 * s, kRows);
-        }
+        mbar_init(b_qfree, 2);
+        mbar_init(b_qtmem, kRows);
+        mbar_init(b_sfull, 1);
+        mbar_init(b_sfree, kRows);
         mbar_init(b_pfull, kRows);
         mbar_init(b_pvdone, 1);
-        mbar_init(b_xfull, kRows);
-        mbar_init(b_xfree, kRows);
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {   // all 512 TMEM columns: scores [0, 128), O [256, 512)
+    if (warp == 1) {   // all 512 TMEM columns: scores, query chunks 0..5, O half
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(
                          smem_u32(&tmem_base)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     tc_fence_before();
-    cluster_sync();   // both ranks' barriers exist before any peer arrive
+    cluster_sync();   // both ranks' barriers and zeroed buffers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t t_s = tmem, t_o = tmem + 256;
+    const uint32_t t_s = tmem + kColS, t_q = tmem + kColQ, t_o = tmem + kColO;
 
     pdl_wait();
     const int total_tiles = a.header[kHdrTotalTiles];
@@ -234,10 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // `site` numbers the wait; a wait that gives up records its bit in the
     // header's wait-site word (diagnostics for VA_ERR_TIMEOUT)
-    auto wait_or_abort = [&](uint32_t bar, uint32_t parity, bool cluster_scope, int site) {
+    auto wait_or_abort = [&](uint32_t bar, uint32_t parity, int site) {
         if (*(volatile int*)&abort_flag) return;
-        const bool ok = cluster_scope ? wait_cluster(bar, parity) : mbar_wait(bar, parity);
-        if (!ok) {
+        if (!mbar_wait(bar, parity)) {
             set_error(a, VA_ERR_TIMEOUT);
             atomicOr(a.header + kHdrWaitSites, 1 << site);
             abort_flag = 1;
@@ -250,174 +257,232 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (warp == 0) {
             // =================== TMA producer (one thread) ===================
+            // rank r issues the 64-column chunks c with c % 2 == r, multicast to both ranks
             if (lane == 0) {
                 int seg = -1;
                 for (int k = 0; k < n_tiles; ++k) {
                     const int st = k % geo.stages;
                     const SeqInfo si = a.seq[cur.b];
-                    if (k == 0 || cur.t == 0) {
-                        ++seg;
-                        if (seg >= 1) wait_or_abort(b_qfree, (seg - 1) & 1, false, 1);
-                        const bool rows = cur.g < si.draft;   // this draft exists
-                        mbar_arrive_expect_tx(b_qfull, rows ? (uint32_t)(n_chunks * kRows * 128) : 0u);
-                        if (rows) {
-                            const int qrow = (si.qoff + cur.g) * a.hq;
-                            for (int c = 0; c < n_chunks; ++c)
-                                tma_2d(smem_u32(qs + c * kRows * 128), &qmap, (c_begin + c) * kChunk, qrow,
-                                       b_qfull);
-                        }
-                    }
-                    if (k >= geo.stages) wait_or_abort(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, false, 2);
-                    // boxes of tb tokens; those wholly outside [lo, P + D) are skipped
+                    // resolve the tile's boxes before waiting for the stage
                     const int j0 = si.a0 + cur.t * kTok;
                     const int end = si.prefix + si.draft;
                     const int indptr = __ldg(a.kv_indptr + cur.b);
+                    int slot[kTok / 8];
                     uint32_t nbox = 0;
-                    for (int j = j0; j < j0 + kTok; j += geo.tb)
-                        if (j < end && j + geo.tb > si.lo) ++nbox;
-                    mbar_arrive_expect_tx(b_kfull + 8 * st, nbox * n_chunks * geo.tb * 128);
-                    unsigned char* const stg = ring + st * stage_bytes;
-                    for (int j = j0; j < j0 + kTok; j += geo.tb) {
-                        if (!(j < end && j + geo.tb > si.lo)) continue;
-                        const int page = __ldg(a.page_table + indptr + j / a.page_size);
-                        if (page < 0 || page >= a.num_pages) {   // counted above: deliver zeros instead
-                            set_error(a, VA_ERR_BAD_PAGE);
-                            // keep the byte count balanced: read the pool's first page
+#pragma unroll
+                    for (int q = 0; q < kTok / 8; ++q) {
+                        const int j = j0 + q * geo.tb;
+                        slot[q] = -1;
+                        if (q * geo.tb < kTok && j < end && j + geo.tb > si.lo) {   // box overlaps [lo, P + D)
+                            const int page = __ldg(a.page_table + indptr + j / a.page_size);
+                            if (page < 0 || page >= a.num_pages) set_error(a, VA_ERR_BAD_PAGE);
+                            // an out-of-range id still delivers its bytes (from page 0) so the count balances
+                            const int pg = (page < 0 || page >= a.num_pages) ? 0 : page;
+                            slot[q] = pg * a.page_size + j % a.page_size;
+                            ++nbox;
                         }
-                        const int pg = (page < 0 || page >= a.num_pages) ? 0 : page;
-                        const int slot = pg * a.page_size + j % a.page_size;
-                        for (int c = 0; c < n_chunks; ++c)
-                            tma_2d(smem_u32(stg + c * kTok * 128 + (j - j0) * 128), &kmap,
-                                   (c_begin + c) * kChunk, slot, b_kfull + 8 * st);
+                    }
+                    if (k == 0 || cur.t == 0) {
+                        ++seg;
+                        if (seg >= 1) wait_or_abort(b_qfree, (seg - 1) & 1, 1);
+                        const bool rows = cur.g < si.draft;   // this draft exists
+                        mbar_arrive_expect_tx(b_qfull, rows ? (uint32_t)kQBytes : 0u);
+                        if (rows) {
+                            const int qrow = (si.qoff + cur.g) * a.hq;
+                            for (int c = kQTmem + (int)rank; c < kChunks; c += 2)
+                                tma_2d_pair(smem_u32(qs + (c - kQTmem) * kRows * 128), &qmap, c * kChunk, qrow,
+                                            b_qfull);
+                        }
+                    }
+                    if (k >= geo.stages) wait_or_abort(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2);
+                    mbar_arrive_expect_tx(b_kfull + 8 * st, nbox * kChunks * geo.tb * 128);
+                    unsigned char* const stg = ring + st * kStageBytes;
+#pragma unroll
+                    for (int q = 0; q < kTok / 8; ++q) {
+                        if (slot[q] < 0) continue;
+                        for (int c = (int)rank; c < kChunks; c += 2)
+                            tma_2d_pair(smem_u32(stg + c * kTok * 128 + q * geo.tb * 128), &kmap, c * kChunk,
+                                        slot[q], b_kfull + 8 * st);
                     }
                     if (k + 1 < n_tiles) cur.advance(a);
                 }
             }
         } else if (warp == 1) {
             // =================== MMA issuer (one thread) ===================
+            // Event-driven: P V of the oldest tile whose P is written goes
+            // first (it frees a KV stage for the producer); otherwise the
+            // scores of the next tile once its stage has landed, the score
+            // columns have been read and (at a segment start) the query is in
+            // place. The scores of tile k + 1 may start before P V of tile k,
+            // so the tensor pipe works on them during tile k's softmax.
             if (lane == 0) {
                 const uint32_t id_s = idesc_bf16(kRows, kTok, 0, 0);
                 const uint32_t id_o = idesc_bf16(kRows, kV / 2, 0, 1);
-                int seg = -1, first_pv = 1;
-                for (int k = 0; k < n_tiles; ++k) {
-                    const int st = k % geo.stages, sb = k & 1;
-                    const bool seg_begin = (k == 0) || (cur.t == 0);
-                    const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
-                    if (seg_begin) {
-                        ++seg;
-                        wait_or_abort(b_qfull, seg & 1, false, 3);
-                        first_pv = 1;
+                // descriptors at offset 0; offsets (>> 4) add into the address field
+                const uint64_t q_desc = sdesc(smem_u32(qs), 16, 1024, 2);
+                const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
+                Cursor qk_cur = cur, pv_cur = cur;
+                int qk_next = 0, pv_next = 0, qk_seg = -1;
+                int idle = 0;
+                long long idle_since = 0;
+                while (pv_next < n_tiles && !*(volatile int*)&abort_flag) {
+                    if (pv_next < qk_next && mbar_test(b_pfull, pv_next & 1)) {
+                        // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
+                        const int k = pv_next, st = k % geo.stages;
+                        const bool first = (k == 0) || (pv_cur.t == 0);
+                        tc_fence_after();
+                        const uint64_t v_desc =
+                            sdesc(smem_u32(ring + st * kStageBytes + rank * 4 * kTok * 128), kTok * 128, 1024, 2);
+#pragma unroll
+                        for (int s4 = 0; s4 < kTok / 16; ++s4)
+                            umma(t_o, p_desc + (uint64_t)((s4 * 32) >> 4), v_desc + (uint64_t)((s4 * 2048) >> 4),
+                                 id_o, !(first && s4 == 0));
+                        umma_commit(b_pvdone);
+                        umma_commit_pair(b_kempty + 8 * st);
+                        if (++pv_next < n_tiles) pv_cur.advance(a);
+                        idle = 0;
+                        continue;
                     }
-                    wait_or_abort(b_kfull + 8 * st, (k / geo.stages) & 1, false, 4);
-                    if (k >= 2) wait_or_abort(b_sfree + 8 * sb, ((k >> 1) - 1) & 1, false, 5);
-                    tc_fence_after();
-                    // partial scores: S_r = Q[:, slice] K[:, slice]^T  (M 128, N 64, K = slice)
-                    const uint32_t kst = smem_u32(ring + st * stage_bytes);
-                    const uint32_t qb = smem_u32(qs);
-                    for (int c = 0; c < n_chunks; ++c)
-                        for (int s = 0; s < 4; ++s)
-                            umma(t_s + sb * kTok, sdesc(qb + c * kRows * 128 + s * 32, 16, 1024),
-                                 sdesc(kst + c * kTok * 128 + s * 32, 16, 1024), id_s, (c | s) != 0);
-                    umma_commit(b_sfull + 8 * sb);
-                    if (seg_end) umma_commit(b_qfree);   // the segment's query slice is no longer read
-                    // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
-                    wait_or_abort(b_pfull, k & 1, false, 6);
-                    tc_fence_after();
-                    for (int s = 0; s < kTok / 16; ++s)
-                        umma(t_o, sdesc(smem_u32(ps) + s * 32, 16, 1024),
-                             sdesc(kst + s * 2048, 64 * 128, 1024), id_o, !(first_pv && s == 0));
-                    first_pv = 0;
-                    umma_commit(b_pvdone);
-                    umma_commit(b_kempty + 8 * st);
-                    if (k + 1 < n_tiles) cur.advance(a);
+                    if (qk_next < n_tiles && qk_next <= pv_next + 1) {
+                        const int k = qk_next, st = k % geo.stages;
+                        const bool seg_begin = (k == 0) || (qk_cur.t == 0);
+                        const bool ready = (!seg_begin || (mbar_test(b_qfull, (qk_seg + 1) & 1) &&
+                                                           mbar_test(b_qtmem, (qk_seg + 1) & 1))) &&
+                                           mbar_test(b_kfull + 8 * st, (k / geo.stages) & 1) &&
+                                           (k == 0 || mbar_test(b_sfree, (k - 1) & 1));
+                        if (ready) {
+                            const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
+                            if (seg_begin) ++qk_seg;
+                            tc_fence_after();
+                            // S = Q K^T  (M 128, N 64, K 576 in 36 steps of 16)
+                            const uint64_t k_desc = sdesc(smem_u32(ring + st * kStageBytes), 16, 1024, 2);
+#pragma unroll
+                            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                                for (int s4 = 0; s4 < 4; ++s4) {
+                                    const uint64_t kd = k_desc + (uint64_t)((c * kTok * 128 + s4 * 32) >> 4);
+                                    if (c < kQTmem)
+                                        umma_ts(t_s, t_q + c * 32 + s4 * 8, kd, id_s, (c | s4) != 0);
+                                    else
+                                        umma(t_s, q_desc + (uint64_t)(((c - kQTmem) * kRows * 128 + s4 * 32) >> 4),
+                                             kd, id_s, 1);
+                                }
+                            umma_commit(b_sfull);
+                            if (seg_end) umma_commit_pair(b_qfree);   // the segment's query is no longer read
+                            if (++qk_next < n_tiles) qk_cur.advance(a);
+                            idle = 0;
+                            continue;
+                        }
+                    }
+                    // nothing ready: a bounded spin (cycle counter, checked every 256 polls)
+                    if (idle++ == 0) idle_since = clock64();
+                    if ((idle & 255) == 0 && clock64() - idle_since > kSpinCycles) {
+                        set_error(a, VA_ERR_TIMEOUT);
+                        atomicOr(a.header + kHdrWaitSites, 1 << 15);
+                        abort_flag = 1;
+                        break;
+                    }
                 }
+                // the peer's last commits land on this CTA's barriers: see them
+                // arrive before the CTA may exit
+                for (int k = n_tiles - geo.stages < 0 ? 0 : n_tiles - geo.stages; k < n_tiles; ++k)
+                    wait_or_abort(b_kempty + 8 * (k % geo.stages), (k / geo.stages) & 1, 12);
+                wait_or_abort(b_qfree, qk_seg & 1, 13);
             }
         } else {
             // =================== softmax warps: thread = row ===================
             const int row = (warp & 3) * 32 + lane;              // TMEM lane quadrant = warp % 4
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t x_mine = smem_u32(xs + row * kXStride);
-            const uint32_t x_peer = map_peer(x_mine, peer);
-            const uint32_t xfull_peer = map_peer(b_xfull, peer);
-            const uint32_t xfree_peer = map_peer(b_xfree, peer);
             float m_ref = -INFINITY, l_sum = 0.f;
             SeqInfo si = {};
+            int seg = -1;
             for (int k = 0; k < n_tiles; ++k) {
-                const int sb = k & 1;
                 const bool seg_begin = (k == 0) || (cur.t == 0);
                 const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
+                const int i = cur.g;   // draft index of this row block: one causal bound for all rows
                 if (seg_begin) {
                     si = a.seq[cur.b];
                     m_ref = -INFINITY;
                     l_sum = 0.f;
+                    ++seg;
+                    // 0. this row's query chunks 0..5 into TMEM once the previous
+                    //    segment's score MMAs are done with them
+                    if (seg >= 1) wait_or_abort(b_qfree, (seg - 1) & 1, 0);
+                    tc_fence_after();
+                    const bool live = i < si.draft;
+                    const uint4* qrow = reinterpret_cast<const uint4*>(
+                        static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)(si.qoff + i) * a.hq + row) * kQk);
+#pragma unroll 1
+                    for (int c = 0; c < kQTmem; ++c) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const uint4 x = live ? __ldg(qrow + c * 8 + v) : make_uint4(0, 0, 0, 0);
+                            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+                        }
+                        VA_TMEM_ST32(t_q + c * 32 + lane_off, r);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                    tc_fence_before();
+                    mbar_arrive(b_qtmem);
                 }
-                const int i = cur.g;   // draft index of this row block
-                const bool live_rows = i < si.draft;
                 const int hi = si.prefix + i;
-                const int lo = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
+                const int lo = max(si.lo, a.window >= 0 ? si.prefix + i - a.window : 0);
                 const int j0 = si.a0 + cur.t * kTok;
                 const int seq_end = si.prefix + si.draft;
+                const bool live_rows = i < si.draft;
 
-                // 1. my partial scores from TMEM
-                wait_or_abort(b_sfull + 8 * sb, (k >> 1) & 1, false, 7);
+                // 1. scores from TMEM
+                wait_or_abort(b_sfull, k & 1, 7);
                 tc_fence_after();
                 float s[kTok];
                 {
                     uint32_t r[32];
-                    VA_TMEM_LD32(t_s + sb * kTok + lane_off, r);
+                    VA_TMEM_LD32(t_s + lane_off, r);
                     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
-                    VA_TMEM_LD32(t_s + sb * kTok + 32 + lane_off, r);
+                    for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]) * a.scale_log2;
+                    VA_TMEM_LD32(t_s + 32 + lane_off, r);
                     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]) * a.scale_log2;
                 }
                 tc_fence_before();
-                mbar_arrive(b_sfree + 8 * sb);
-                // 2. send them to the peer, receive the peer's, add (identical on both ranks)
-                if (k >= 1) wait_or_abort(b_xfree, (k - 1) & 1, true, 8);
+                mbar_arrive(b_sfree);
+                // 2. mask (the same for every row of the block) and online softmax
+                //    in base 2 with lazy rescaling by 2^8
+                if (!live_rows || j0 < lo || j0 + kTok - 1 > hi) {
 #pragma unroll
-                for (int j = 0; j < kTok; j += 4) st_peer_v4(x_peer + j * 4, s[j], s[j + 1], s[j + 2], s[j + 3]);
-                arrive_peer(xfull_peer);
-                wait_or_abort(b_xfull, k & 1, true, 9);
-#pragma unroll
-                for (int j = 0; j < kTok; j += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(xs + row * kXStride + j * 4);
-                    // same operand order on both ranks: rank 0's slice + rank 1's slice
-                    if (rank == 0) {
-                        s[j] += v.x; s[j + 1] += v.y; s[j + 2] += v.z; s[j + 3] += v.w;
-                    } else {
-                        s[j] = v.x + s[j]; s[j + 1] = v.y + s[j + 1]; s[j + 2] = v.z + s[j + 2]; s[j + 3] = v.w + s[j + 3];
+                    for (int j = 0; j < kTok; ++j) {
+                        const int t = j0 + j;
+                        if (!live_rows || t > hi || t < lo) s[j] = -INFINITY;
                     }
                 }
-                arrive_peer(xfree_peer);
-                // 3. mask and online softmax (base 2, lazy rescale by 2^8)
-                float mx = -INFINITY;
+                float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) {
-                    const int t = j0 + j;
-                    const float v = (live_rows && t <= hi && t >= lo && t >= si.lo) ? s[j] * a.scale_log2 : -INFINITY;
-                    s[j] = v;
-                    mx = fmaxf(mx, v);
+                for (int j = 4; j < kTok; j += 4) {
+                    mx[0] = fmaxf(mx[0], s[j]);
+                    mx[1] = fmaxf(mx[1], s[j + 1]);
+                    mx[2] = fmaxf(mx[2], s[j + 2]);
+                    mx[3] = fmaxf(mx[3], s[j + 3]);
                 }
-                const bool rescale = mx > m_ref + 8.f;
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const bool rescale = m_tile > m_ref + 8.f;
                 float alpha = 1.f;
                 if (rescale) {
-                    alpha = exp2f(m_ref - mx);   // 0 when m_ref is -inf
-                    m_ref = mx;
+                    alpha = ex2_approx(m_ref - m_tile);   // 0 when m_ref is -inf
+                    m_ref = m_tile;
                 }
                 const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-                float psum = 0.f;
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < kTok; ++j) {
-                    const float p = exp2f(s[j] - mu);
-                    s[j] = p;
-                    psum += p;
+                    s[j] = ex2_approx(s[j] - mu);
+                    ps4[j & 3] += s[j];
                 }
-                l_sum = l_sum * alpha + psum;
-                // 4. the previous PV must be done before P is rewritten or O rescaled
-                if (k >= 1) wait_or_abort(b_pvdone, (k - 1) & 1, false, 10);
+                l_sum = l_sum * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+                // 3. the previous P V must be done before P is rewritten or O rescaled
+                if (k >= 1) wait_or_abort(b_pvdone, (k - 1) & 1, 10);
                 tc_fence_after();
                 // tcgen05.ld / st are warp-collective: the warp rescales if any of
                 // its rows needs it (the others multiply by alpha = 1)
@@ -434,16 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
                 }
                 // V rows of tokens past the sequence end may hold garbage: zero
-                // this rank's V columns there (0 * NaN would poison P V)
+                // this rank's V chunks there (0 * NaN would poison P V)
                 if (j0 + kTok > seq_end) {
-                    unsigned char* stg = ring + (k % geo.stages) * stage_bytes;
-                    const int t = row & 63, half = row >> 6;     // two rows per token
-                    if (j0 + t >= seq_end)
-                        for (int c = half * 2; c < half * 2 + 2; ++c)
+                    const int t = row & (kTok - 1);
+                    if (j0 + t >= seq_end) {
+                        unsigned char* const stg = ring + (k % geo.stages) * kStageBytes + t * 128;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {   // 4 chunks x 64 tokens over 128 threads
+                            const int c = (int)rank * 4 + (row >> 6) * 2 + h;
+#pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                *reinterpret_cast<uint4*>(stg + c * kTok * 128 + t * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+                                reinterpret_cast<uint4*>(stg + c * kTok * 128)[q] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
                 }
-                // 5. P (bf16) into the K-major swizzled A operand: row `row`, 64 tokens = 128 bytes
+                // 4. P (bf16) into the K-major swizzled A operand: row `row`, 64 tokens = 128 bytes
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     uint32_t w[4];
@@ -457,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(b_pfull);
-                // 6. segment end: normalised partial output of this rank's v half
+                // 5. segment end: normalised partial output of this rank's v half
                 if (seg_end) {
-                    wait_or_abort(b_pvdone, k & 1, false, 11);
+                    wait_or_abort(b_pvdone, k & 1, 11);
                     tc_fence_after();
                     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
                     const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
@@ -483,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    // teardown: every MMA has been waited on by the softmax warps (pv_done of
-    // the last tile); no peer access after the cluster barrier
+    // teardown: every MMA of this CTA has been waited on (pv_done of its last
+    // tile), and the peer's multicast commits to this CTA have arrived
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -528,15 +598,12 @@ int gcd_i(int x, int y) {
 
 bool mla_available() { return true; }
 
-// Shared-memory bytes of rank 1 (the larger) for `stages` KV stages.
-static int mla_smem(int stages) {
-    const int q = 5 * kRows * 128, st = 5 * kTok * 128;
-    return 1024 + q + stages * st + kRows * 128 + kRows * kXStride + 256;
-}
+// Shared-memory bytes for `stages` KV stages (alignment slack, Q, ring, P, barriers).
+static int mla_smem(int stages) { return 1024 + kQBytes + stages * kStageBytes + kPBytes + 256; }
 
 int mla_stages() {
-    int s = 4;
-    while (s > 1 && mla_smem(s) > 227 * 1024 - 64) --s;
+    int s = 4;   // the kernel's static shared memory (1 KB with the aligned dynamic base) counts too
+    while (s > 1 && mla_smem(s) > 227 * 1024 - 1024 - 64) --s;
     return s;
 }
 
