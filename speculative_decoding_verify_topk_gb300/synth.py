@@ -225,6 +225,26 @@ def paginate(lg: Logical, page_size: int | None = None, pool_pages: int | None =
                  lg.seq_lens.to(device), lg.num_draft.to(device), ps)
 
 
+def token_indices(pb: Paged):
+    """The batch's KV addressing in the token-level form a serving stack holds:
+    kv_indptr_tok [bs + 1] (token offsets, T_b = P_b + D_b tokens per
+    sequence) and kv_indices [sum T_b], the pool slot page * page_size + row of
+    every logical token (CPU int32 tensors)."""
+    ps = pb.page_size
+    t = (pb.seq_lens.cpu().to(torch.int64) + pb.num_draft.cpu().to(torch.int64))
+    indptr = pb.kv_indptr.cpu().to(torch.int64)
+    table = pb.page_table.cpu().to(torch.int64)
+    tok_indptr = torch.zeros(len(t) + 1, dtype=torch.int64)
+    tok_indptr[1:] = torch.cumsum(t, 0)
+    slots = []
+    for b in range(len(t)):
+        j = torch.arange(int(t[b]), dtype=torch.int64)
+        pages = table[int(indptr[b]):int(indptr[b + 1])]
+        slots.append(pages[j // ps] * ps + j % ps)
+    slots = torch.cat(slots) if slots else torch.zeros(0, dtype=torch.int64)
+    return tok_indptr.to(torch.int32), slots.to(torch.int32)
+
+
 def make_batch(name_or_wl, device="cpu", seed: int | None = None, **overrides) -> Paged:
     wl = WORKLOADS[name_or_wl] if isinstance(name_or_wl, str) else name_or_wl
     if overrides:
