@@ -441,10 +441,13 @@ def ours_arm(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / e2e_steps}
 
+    builder = time_page_table_builder(pb, stream, dev, flush)
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
+    if builder is not None:
+        builder["frac_of_measured_hbm"] = builder["gbs"] / hbm_peak
     prefix_avg_ms = statistics.fmean(prefix_ms)
     kernel = {va.VA_PATH_MMA: "prefix_mma", va.VA_PATH_F32: "prefix_f32",
               va.VA_PATH_MLA: "prefix_mla"}[attn.plan.path]
@@ -490,10 +493,50 @@ def ours_arm(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "page_table_builder": builder,
         "gpu_launches": attn.launches_per_call * steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def time_page_table_builder(pb, stream, dev, flush, steps: int = 200):
+    """Times verify_attn_build_page_table on the batch's token-level indices (the
+    step a serving stack runs before the call); cold L2 between calls. Returns
+    its mean time and algorithmic bytes (every token index read once, every
+    page entry, kv_indptr and seq_len written once), or None for an empty batch."""
+    import speculative_decoding_verify_topk_gb300 as va
+    tok_indptr, slots = synth.token_indices(pb)
+    bs = int(pb.seq_lens.numel())
+    if slots.numel() == 0:
+        return None
+    t_indptr, t_slots = tok_indptr.to(dev), slots.to(dev)
+    cap = int(pb.kv_indptr[-1])
+    pages_indptr = torch.empty(bs + 1, dtype=torch.int32, device=dev)
+    table = torch.empty(cap, dtype=torch.int32, device=dev)
+    seq_lens = torch.empty(bs, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def build():
+        va.verify_attn_build_page_table(bs, pb.page_size, pb.num_pages, t_indptr, t_slots, pb.num_draft,
+                                        pages_indptr, table, cap, 0, seq_lens, err, stream=stream)
+    for _ in range(3):
+        build()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        build()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ok = (int(err.item()) == 0 and torch.equal(table, pb.page_table)
+          and torch.equal(pages_indptr, pb.kv_indptr) and torch.equal(seq_lens, pb.seq_lens))
+    ms = statistics.fmean(times)
+    nbytes = 4 * (int(slots.numel()) + (bs + 1) * 2 + cap + 2 * bs)
+    return {"us_per_call": ms * 1e3, "bytes_per_call": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "launches_per_call": 2, "steps": steps, "table_matches_batch": bool(ok)}
 
 
 def main():

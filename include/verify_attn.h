@@ -233,6 +233,53 @@ int verify_attn_paged_static(const va_plan *plan, int bs, const void *q, const v
                              const int32_t *num_draft, int page_size, float scale, int window,
                              void *out, float *lse, void *stream);
 
+/*
+ * Builds the page-level table verify_attn_paged reads from token-level KV
+ * indices, on the device. Source: "[AMD] Enable EAGLE speculative decoding for
+ * Qwen3.5 FP8 and MXFP4 models with aiter's unified attention", Modifications:
+ * the speculative paths hold token-level ragged indices while the paged kernel
+ * wants a block table, which two small kernels build without a
+ * bs x max_context scratch; each row's KV length is taken from kv_indptr.
+ *
+ *   bs              sequences (0 returns VA_OK and launches nothing)
+ *   page_size       tokens per page of the pool (>= 1)
+ *   num_pages       pages in the pool (slots >= num_pages * page_size are errors)
+ *   kv_indptr_tok   int32 [bs + 1]: sequence b's KV tokens (prefix and drafts,
+ *                   T_b = P_b + D_b of them) are kv_indices[kv_indptr_tok[b] ..
+ *                   kv_indptr_tok[b + 1])
+ *   kv_indices      int32: each token's pool slot, page * page_size + row; token
+ *                   j of a sequence must sit at row j % page_size of the page
+ *                   that holds its logical page j / page_size
+ *   num_draft       int32 [bs] (D_b) or NULL
+ *   kv_indptr_pages int32 [bs + 1], written: the page-level kv_indptr
+ *   page_table      int32 [capacity], written: page_table[kv_indptr_pages[b] + k]
+ *                   = page of sequence b's logical page k (-1 if that page's
+ *                   first slot lies outside the pool)
+ *   capacity        entries page_table holds
+ *   row_stride      0: packed CSR (kv_indptr_pages is the exclusive scan of
+ *                   ceil(T_b / page_size)); > 0: padded 2-D table [bs, row_stride]
+ *                   (kv_indptr_pages[b] = b * row_stride; entries past a
+ *                   sequence's pages are left untouched)
+ *   seq_lens        int32 [bs], written (may be NULL; needs num_draft):
+ *                   P_b = T_b - D_b, the verify call's seq_lens
+ *   error_word      int32 device word, overwritten with the bits of this call:
+ *                   VA_ERR_BAD_PAGE (a slot outside the pool, off its row, or in
+ *                   another page than the first token of its logical page),
+ *                   VA_ERR_SHORT_TABLE (the table does not fit capacity or
+ *                   row_stride), VA_ERR_BAD_LENGTH (kv_indptr_tok decreasing, or
+ *                   num_draft[b] outside [0, T_b]; such a sequence counts as
+ *                   empty and its seq_len is 0)
+ *   stream          cudaStream_t
+ *
+ * All buffers are device memory owned by the caller; nothing is allocated and
+ * nothing synchronises. Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
+ */
+int verify_attn_build_page_table(int bs, int page_size, int64_t num_pages,
+                                 const int32_t *kv_indptr_tok, const int32_t *kv_indices,
+                                 const int32_t *num_draft, int32_t *kv_indptr_pages,
+                                 int32_t *page_table, int64_t capacity, int row_stride,
+                                 int32_t *seq_lens, int32_t *error_word, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

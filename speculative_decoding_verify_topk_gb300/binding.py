@@ -20,7 +20,7 @@ VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
-           "verify_attn_paged_static", "verify_attn_last_error")
+           "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table")
 
 
 class Problem(ctypes.Structure):
@@ -88,6 +88,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.verify_attn_last_error.restype = ctypes.c_char_p
         lib.verify_attn_launches_per_call.argtypes = [ctypes.POINTER(Plan)]
         lib.verify_attn_launches_per_call.restype = I
+        L = ctypes.c_int64
+        lib.verify_attn_build_page_table.argtypes = [I, I, L, P, P, P, P, P, L, I, P, P, P]
+        lib.verify_attn_build_page_table.restype = I
         _lib = lib
         return lib
 
@@ -160,3 +163,17 @@ def verify_attn_check(plan: Plan, workspace, stream=None) -> int:
 
 def verify_attn_launches_per_call(plan: Plan) -> int:
     return load_library().verify_attn_launches_per_call(ctypes.byref(plan))
+
+
+def verify_attn_build_page_table(bs: int, page_size: int, num_pages: int, kv_indptr_tok, kv_indices,
+                                 num_draft, kv_indptr_pages, page_table, capacity: int,
+                                 row_stride: int, seq_lens, error_word, stream=None) -> None:
+    """Calls verify_attn_build_page_table (device tensors by data_ptr(); num_draft
+    and seq_lens may be None); raises VerifyAttnError on a nonzero status. The
+    device error bits land in error_word."""
+    rc = load_library().verify_attn_build_page_table(
+        int(bs), int(page_size), int(num_pages), _ptr(kv_indptr_tok), _ptr(kv_indices), _ptr(num_draft),
+        _ptr(kv_indptr_pages), _ptr(page_table), int(capacity), int(row_stride), _ptr(seq_lens),
+        _ptr(error_word), _stream_handle(stream))
+    if rc != VA_OK:
+        raise VerifyAttnError(rc, "verify_attn_build_page_table")

@@ -364,6 +364,12 @@ extern "C" int verify_attn_check(const va_plan* plan, const void* workspace, voi
 
 extern "C" const char* verify_attn_last_error(void) { return g_last_error; }
 
+namespace va {
+// Records a failed CUDA step for verify_attn_last_error(); used by the other
+// translation units of the library. Returns VA_CUDA_ERROR.
+int record_cuda_failure(const char* step, cudaError_t e) { return cuda_failure(step, e); }
+}  // namespace va
+
 extern "C" int verify_attn_launches_per_call(const va_plan* plan) {
     return plan ? 3 : 0;
 }
