@@ -73,7 +73,7 @@ def _lib(mutant: int = 0, out_dir: str | None = None) -> ctypes.CDLL:
             f.restype = ctypes.c_int
             P = ctypes.c_void_p
             f.argtypes = [ctypes.c_int] * 7 + [P, P, P, ctypes.c_int, P, P, ctypes.c_int64,
-                                               P, P, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                               P, P, ctypes.c_double, ctypes.c_int, P, ctypes.c_int,
                                                P, ctypes.c_int64, P, P, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_mutant_id.restype = ctypes.c_int
@@ -106,7 +106,8 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
                 num_q_heads: int, num_kv_heads: int, qk_dim: int, v_dim: int, page_size: int,
                 dtype: int, scale: float, window: int = -1, v_aliases_k: bool = False,
                 num_pages: int | None = None, num_splits: int = 1, rows=None,
-                threads: int = 0, mutant: int = 0, mutant_dir: str | None = None):
+                threads: int = 0, mutant: int = 0, mutant_dir: str | None = None,
+                tree_mask=None):
     """Verify attention in fp64.
 
     Arguments follow the C entry point ``verify_attn_paged`` (same meaning and
@@ -114,6 +115,10 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
     v_cache [pages, page_size, Hkv, Dv] (ignored when ``v_aliases_k``);
     page_table / kv_indptr CSR over pages; seq_lens = prefix lengths P_b;
     num_draft = D_b. 16-bit inputs are passed as their bit patterns (uint16).
+
+    ``tree_mask`` (tree verify, topk > 1): None for causal rows, else uint32
+    [sum D_b]; bit d of row i's word means the row sees draft d (every prefix
+    key stays visible; window must be < 0).
 
     ``rows`` None computes every row and returns (out [sum D_b, Hq, Dv],
     lse [sum D_b, Hq]); otherwise an [n, 3] array of (b, i, h) and the result
@@ -144,12 +149,16 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
         lse = np.empty((n_rows,), dtype=np.float64)
     if q.size < total_q * num_q_heads * qk_dim:
         raise ValueError("q is smaller than sum(num_draft) * Hq * Dqk")
+    if tree_mask is not None:
+        tree_mask = np.ascontiguousarray(np.asarray(tree_mask).astype(np.int64).astype(np.uint32))
+        if tree_mask.shape[0] < total_q:
+            raise ValueError("tree_mask needs one word per query row")
     ptr = lambda a: None if a is None else a.ctypes.data
     rc = lib.oracle_verify_attn(bs, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size, dtype,
                                 ptr(q), ptr(k_cache), ptr(v_cache), int(bool(v_aliases_k)),
                                 ptr(page_table), ptr(kv_indptr), int(num_pages),
                                 ptr(seq_lens), ptr(num_draft), float(scale), int(window),
-                                int(num_splits), ptr(rows_arr), int(n_rows),
+                                ptr(tree_mask), int(num_splits), ptr(rows_arr), int(n_rows),
                                 ptr(out), ptr(lse), int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected its input: {_ERRORS.get(rc, rc)}")

@@ -34,6 +34,14 @@
  *    page_table[kv_indptr[b] + k].
  *  - lse is the natural logarithm of sum_j exp(scale * q . k_j).
  *  - Absorbed MLA (v_aliases_k): V is the first Dv entries of the K row.
+ *  - Tree verify (topk > 1, the follow-up the split-KV page defers; its
+ *    baseline applies the tree's custom mask): when tree_mask is given, row i
+ *    of sequence b sees every prefix key 0 .. P_b - 1 and the draft key
+ *    P_b + d exactly when bit d of tree_mask[qoff_b + i] is set (d < D_b; an
+ *    EAGLE tree row sees its ancestors and itself); the drafts keep their
+ *    logical positions P_b .. P_b + D_b - 1 in the page table. A sliding window
+ *    is not defined for tree rows (window must be < 0). A row that sees no key
+ *    at all gives out = 0 and lse = -inf.
  *
  * Arithmetic: every input element is decoded to double exactly (fp32, bf16
  * and fp16 all embed exactly in binary64), and all sums, the exponentials and
@@ -115,6 +123,7 @@ typedef struct {
     double scale;
     const void *q, *k, *v;
     const int32_t *page_table, *kv_indptr, *seq_lens, *num_draft;
+    const uint32_t *tree_mask;   /* NULL: causal */
     const int64_t *qoff;
 } problem;
 
@@ -166,6 +175,10 @@ static double attend_range(const problem *pb, int b, int g, const double *s,
     int d;
     for (j = j0; j < j1; ++j)
         if (s[j - lo] > m) m = s[j - lo];
+    if (m == -INFINITY) { /* no visible key in the range (tree rows only) */
+        for (d = 0; d < pb->dv; ++d) o[d] = 0.0;
+        return -INFINITY;
+    }
     for (j = j0; j < j1; ++j)
         sum += exp(s[j - lo] - m);
 #if ORACLE_MUTANT == 5
@@ -205,6 +218,7 @@ static int one_row(const problem *pb, int b, int i, int h, double *out_row, doub
 #else
     if (pb->window >= 0) lo = p - pb->window > 0 ? p - pb->window : 0;
 #endif
+    if (pb->tree_mask) hi = (int64_t)pb->seq_lens[b] + pb->num_draft[b]; /* the mask picks the drafts */
     n = hi - lo;
     if (n <= 0) { /* only reachable through a planted mistake */
         for (d = 0; d < pb->dv; ++d) out_row[d] = NAN;
@@ -214,6 +228,20 @@ static int one_row(const problem *pb, int b, int i, int h, double *out_row, doub
     for (j = lo; j < hi; ++j) {
         int64_t slot = slot_of(pb, b, j);
         double dot = 0.0;
+        if (pb->tree_mask && j >= pb->seq_lens[b]) {
+            const uint32_t bits = pb->tree_mask[pb->qoff[b] + i];
+#if ORACLE_MUTANT == 10
+            const int64_t dj = j - pb->seq_lens[b] + 1; /* planted: bit index off by one */
+#else
+            const int64_t dj = j - pb->seq_lens[b];
+#endif
+#if ORACLE_MUTANT == 11
+            const int seen = j <= p; /* planted: ignores the tree, keeps the causal chain */
+#else
+            const int seen = dj < 32 && ((bits >> dj) & 1u);
+#endif
+            if (!seen) { s[j - lo] = -INFINITY; continue; }
+        }
         for (d = 0; d < pb->dqk; ++d)
             dot += elem(pb->q, pb->dtype, qrow * pb->dqk + d) * key_elem(pb, slot, kv_head_of(pb, h), d);
 #if ORACLE_MUTANT == 3
@@ -242,6 +270,13 @@ static int one_row(const problem *pb, int b, int i, int h, double *out_row, doub
                 for (d = 0; d < pb->dv; ++d) o_s[(size_t)k * pb->dv + d] = 0.0;
             }
             if (lse_s[k] > big) big = lse_s[k];
+        }
+        if (big == -INFINITY) { /* no visible key at all */
+            for (d = 0; d < pb->dv; ++d) out_row[d] = 0.0;
+            *lse_out = -INFINITY;
+            free(lse_s);
+            free(o_s);
+            return ORACLE_OK;
         }
         for (k = 0; k < S; ++k) acc += exp(lse_s[k] - big);
         lse = big + log(acc);
@@ -293,7 +328,9 @@ static int check_tables(const problem *pb)
  *   page_table  int32, CSR over pages; kv_indptr int32 [bs + 1]
  *   seq_lens    int32 [bs] prefix lengths; num_draft int32 [bs]
  *   dtype       0 fp32, 1 bf16, 2 fp16 (q, k_cache and v_cache share it)
- *   window      < 0: no window
+ *   window      < 0: no window (required with tree_mask)
+ *   tree_mask   NULL: causal rows; else uint32 [sum D_b], bit d of row i's word:
+ *               the row sees draft d (tree verify)
  *   rows        NULL: compute every (b, i, h) into out [sum D_b, hq, dv] and
  *               lse [sum D_b, hq]; otherwise n_rows triples (b, i, h) and the
  *               results go to out [n_rows, dv], lse [n_rows].
@@ -304,8 +341,8 @@ int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, 
                        const void *q, const void *k_cache, const void *v_cache, int v_aliases_k,
                        const int32_t *page_table, const int32_t *kv_indptr, int64_t num_pages,
                        const int32_t *seq_lens, const int32_t *num_draft, double scale, int window,
-                       int num_splits, const int32_t *rows, int64_t n_rows, double *out,
-                       double *lse, int threads)
+                       const uint32_t *tree_mask, int num_splits, const int32_t *rows, int64_t n_rows,
+                       double *out, double *lse, int threads)
 {
     problem pb;
     int64_t *qoff, total_q = 0, r, nr;
@@ -316,6 +353,7 @@ int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, 
         return ORACLE_BAD_ARG;
     if (dtype < ORACLE_F32 || dtype > ORACLE_F16) return ORACLE_BAD_ARG;
     if (v_aliases_k && dv > dqk) return ORACLE_BAD_ARG;
+    if (tree_mask && window >= 0) return ORACLE_BAD_ARG;
     if (bs == 0) return ORACLE_OK;
 
     pb.bs = bs; pb.hq = hq; pb.hkv = hkv; pb.dqk = dqk; pb.dv = dv;
@@ -323,7 +361,7 @@ int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, 
     pb.window = window; pb.num_splits = num_splits; pb.num_pages = num_pages;
     pb.scale = scale; pb.q = q; pb.k = k_cache; pb.v = v_cache;
     pb.page_table = page_table; pb.kv_indptr = kv_indptr;
-    pb.seq_lens = seq_lens; pb.num_draft = num_draft;
+    pb.seq_lens = seq_lens; pb.num_draft = num_draft; pb.tree_mask = tree_mask;
 
     status = check_tables(&pb);
     if (status != ORACLE_OK) return status;

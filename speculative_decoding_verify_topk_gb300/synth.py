@@ -80,6 +80,13 @@ WORKLOADS = {
     "mixed_serving": Workload("mixed_serving", torch.bfloat16, 128, 64, 8, 192, 128, 16,
                               ("lognormal", 2048.0, 1.0, 1, 65536), ("choice", [2, 3, 4, 5]), 4,
                               1.0 / math.sqrt(192), window=(-1, 4096)),
+    # draft-extend after verification ("Support overlap-spec-v2 with fa3 attention
+    # backend"): each sequence's query rows are its accepted tokens plus the
+    # bonus token (1 .. num_draft_tokens + 1 = 5), already written to the cache
+    # behind the committed prefix; the same causal call with ragged rows
+    "draft_extend": Workload("draft_extend", torch.bfloat16, 64, 32, 8, 128, 128, 16,
+                             ("uniform", 1024, 8192), ("choice", [1, 2, 3, 4, 5]), 5,
+                             1.0 / math.sqrt(128)),
 }
 
 
@@ -223,6 +230,39 @@ def paginate(lg: Logical, page_size: int | None = None, pool_pages: int | None =
         v_cache.view(-1, hkv, wl.v_dim).index_copy_(0, slots, lg.v.to(device))
     return Paged(wl, lg.q.to(device), k_cache, v_cache, page_table.to(device), kv_indptr.to(device),
                  lg.seq_lens.to(device), lg.num_draft.to(device), ps)
+
+
+def draft_trees(num_draft, seed: int = 0, shape: str = "random"):
+    """Draft-token trees for tree verify (topk > 1): per sequence a parent list
+    over its D_b drafts (-1 = hangs off the committed prefix, else an earlier
+    draft). shape "random" draws each parent uniformly from -1 .. d - 1,
+    "chain" is the topk = 1 chain, "star" hangs every draft off the prefix."""
+    g = _gen(seed + 7919, "cpu")
+    parents = []
+    for d_b in (int(x) for x in num_draft):
+        par = []
+        for d in range(d_b):
+            if shape == "chain":
+                par.append(d - 1)
+            elif shape == "star":
+                par.append(-1)
+            else:
+                par.append(int(torch.randint(-1, d, (1,), generator=g)) if d > 0 else -1)
+        parents.append(par)
+    return parents
+
+
+def tree_masks(parents):
+    """The call's tree_mask input: int32 [sum D_b], one word per query row with
+    bit d set when the row's draft has draft d as an ancestor or is d."""
+    words = []
+    for par in parents:
+        m = []
+        for d, p in enumerate(par):
+            m.append((1 << d) | (m[p] if p >= 0 else 0))
+        words.extend(m)
+    # the 32-bit words as int32 (two's complement for bit 31)
+    return torch.tensor([x - (1 << 32) if x >= (1 << 31) else x for x in words], dtype=torch.int32)
 
 
 def token_indices(pb: Paged):

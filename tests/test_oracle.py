@@ -204,9 +204,44 @@ def pin_row_select(m=0, d=None):
         assert np.array_equal(sel_o[n], full_o[qoff[b] + i, h]) and sel_l[n] == full_l[qoff[b] + i, h]
 
 
+def pin_tree_brute_force(m=0, d=None):
+    """Tree verify: random draft trees (up to 9 drafts), against the dense brute
+    force whose mask walks the parent pointers."""
+    for dtype in (torch.float32, torch.bfloat16):
+        wl = synth.WORKLOADS["tiny"].replace(dtype=dtype, bs=4, prefix=("fixed", [0, 5, 40, 77]),
+                                             draft=("choice", [1, 4, 7, 9]), pool_tokens=None)
+        lg = synth.make_logical(wl)
+        pb = synth.paginate(lg, page_size=3)
+        for shape in ("random", "star"):
+            parents = synth.draft_trees(lg.num_draft.tolist(), seed=3, shape=shape)
+            out, lse = oracle_on(pb, tree_mask=synth.tree_masks(parents).numpy(), mutant=m, mutant_dir=d)
+            bo, bl = brute_force(lg, tree_parents=parents)
+            _close(out, bo, 1e-12, f"tree out {dtype} {shape}")
+            _close(lse, bl, 1e-12, f"tree lse {dtype} {shape}")
+
+
+def pin_tree_chain_is_causal(m=0, d=None):
+    """A chain tree (the topk = 1 case) gives the causal rows bit for bit."""
+    lg, pb = _pin_batch()
+    chain = synth.tree_masks(synth.draft_trees(lg.num_draft.tolist(), shape="chain")).numpy()
+    t_o, t_l = oracle_on(pb, tree_mask=chain, mutant=m, mutant_dir=d)
+    c_o, c_l = oracle_on(pb, mutant=m, mutant_dir=d)
+    assert np.array_equal(t_o, c_o) and np.array_equal(t_l, c_l), "chain tree differs from causal"
+
+
+def pin_tree_split_invariance(m=0, d=None):
+    lg, pb = _pin_batch()
+    masks = synth.tree_masks(synth.draft_trees(lg.num_draft.tolist(), seed=5)).numpy()
+    base = oracle_on(pb, tree_mask=masks, mutant=m, mutant_dir=d)
+    for s in (3, 17):
+        out, lse = oracle_on(pb, tree_mask=masks, num_splits=s, mutant=m, mutant_dir=d)
+        _close(out, base[0], 1e-12, f"tree out S={s}")
+        _close(lse, base[1], 1e-12, f"tree lse S={s}")
+
+
 PINS = [pin_brute_force, pin_sdpa, pin_page_size_invariance, pin_split_invariance, pin_equal_keys,
         pin_single_key, pin_window_cases, pin_gqa_mapping, pin_mla_alias, pin_decoders,
-        pin_row_select]
+        pin_row_select, pin_tree_brute_force, pin_tree_chain_is_causal, pin_tree_split_invariance]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -226,7 +261,16 @@ MUTANTS = {
     7: ("query row ignores earlier sequences", {"pin_brute_force", "pin_sdpa"}),
     8: ("split pieces merged without lse weights", {"pin_split_invariance"}),
     9: ("values read from the K pool instead of V", {"pin_brute_force", "pin_sdpa"}),
+    10: ("tree mask bit index off by one", {"pin_tree_brute_force", "pin_tree_chain_is_causal"}),
+    11: ("tree mask ignored (causal chain kept)", {"pin_tree_brute_force"}),
 }
+
+
+def test_tree_rejects_window():
+    lg, pb = _pin_batch()
+    masks = synth.tree_masks(synth.draft_trees(lg.num_draft.tolist())).numpy()
+    with pytest.raises(ValueError):
+        oracle_on(pb, window=3, tree_mask=masks)
 
 
 @pytest.fixture(scope="module")

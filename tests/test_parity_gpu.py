@@ -61,10 +61,25 @@ def small(name, **over):
     base = {"llama8b_gqa": dict(bs=5, prefix=("uniform", 60, 700)),
             "long_context": dict(bs=3, prefix=("uniform", 900, 2500)),
             "mixed_serving": dict(bs=9, prefix=("lognormal", 200.0, 1.0, 1, 1500)),
-            "dsv3_mla": dict(bs=3, prefix=("uniform", 100, 900))}[name]
+            "dsv3_mla": dict(bs=3, prefix=("uniform", 100, 900)),
+            "draft_extend": dict(bs=12, prefix=("uniform", 0, 600))}[name]
     base.update(over)
     wl = synth.WORKLOADS[name].replace(pool_tokens=None, **base)
     return wl
+
+
+@pytest.mark.parametrize("window", [-1, 50])
+def test_draft_extend_ragged_rows(window):
+    """Draft-extend shape: 1 .. 5 query rows per sequence (accepted tokens plus
+    the bonus token), page size 16, some empty prefixes."""
+    check(synth.make_batch(small("draft_extend")), window=window)
+
+
+def test_draft_extend_with_rowless_sequences():
+    """Sequences with no query rows this step sit between sequences with rows."""
+    wl = small("draft_extend", bs=6)
+    lg = synth.make_logical(wl, seq_lens=[300, 41, 0, 700, 64, 5], num_draft=[3, 0, 1, 0, 5, 2])
+    check(synth.paginate(lg), max_draft=5)
 
 
 def test_tiny_fp32():

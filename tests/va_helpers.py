@@ -11,7 +11,7 @@ from speculative_decoding_verify_topk_gb300 import synth
 
 
 def oracle_on(pb: synth.Paged, window: int = -1, num_splits: int = 1, rows=None,
-              threads: int = 0, mutant: int = 0, mutant_dir=None, scale=None):
+              threads: int = 0, mutant: int = 0, mutant_dir=None, scale=None, tree_mask=None):
     wl = pb.wl
     return oracle.verify_attn(
         synth.raw_bits(pb.q), synth.raw_bits(pb.k_cache),
@@ -22,12 +22,16 @@ def oracle_on(pb: synth.Paged, window: int = -1, num_splits: int = 1, rows=None,
         v_dim=wl.v_dim, page_size=pb.page_size, dtype=synth.DTYPE_CODES[wl.dtype],
         scale=wl.scale if scale is None else scale, window=window,
         v_aliases_k=wl.v_aliases_k, num_pages=pb.num_pages, num_splits=num_splits,
-        rows=rows, threads=threads, mutant=mutant, mutant_dir=mutant_dir)
+        rows=rows, threads=threads, mutant=mutant, mutant_dir=mutant_dir,
+        tree_mask=None if tree_mask is None else np.asarray(tree_mask).astype(np.int64) & 0xFFFFFFFF)
 
 
-def brute_force(lg: synth.Logical, window: int = -1, scale=None):
+def brute_force(lg: synth.Logical, window: int = -1, scale=None, tree_parents=None):
     """Dense attention straight from the contiguous per-sequence K/V: the full
-    D_b x T_b score matrix with an explicit boolean mask, then a softmax."""
+    D_b x T_b score matrix with an explicit boolean mask, then a softmax.
+    With tree_parents (per sequence a parent list over its drafts), a draft row
+    sees the whole prefix and the drafts on its path to the prefix, found by
+    walking the parent pointers."""
     wl = lg.wl
     scale = wl.scale if scale is None else scale
     q = lg.q.double().cpu().numpy()
@@ -43,6 +47,14 @@ def brute_force(lg: synth.Logical, window: int = -1, scale=None):
         allowed = key <= pos
         if window >= 0:
             allowed &= key >= pos - window
+        if tree_parents is not None:
+            allowed = np.zeros((d_b, t1 - t0), dtype=bool)
+            allowed[:, :p_b] = True
+            for i in range(d_b):
+                node = i
+                while node >= 0:
+                    allowed[i, p_b + node] = True
+                    node = tree_parents[b][node]
         o_b = np.empty((d_b, wl.num_q_heads, wl.v_dim))
         l_b = np.empty((d_b, wl.num_q_heads))
         for h in range(wl.num_q_heads):
