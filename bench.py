@@ -74,7 +74,7 @@ def parse():
 # algorithmic bytes / flops
 # ---------------------------------------------------------------------------
 
-def call_accounting(pb: synth.Paged, window: int):
+def call_accounting(pb: synth.Paged, window: int, tree=None):
     """Algorithmic bytes of one call and of its prefix kernel.
 
     KV: every key token any row can see, once per kv-head: keys [lo_b, P_b + D_b)
@@ -96,6 +96,17 @@ def call_accounting(pb: synth.Paged, window: int):
     lse_bytes = rows * 4
     # flops: every (row, visible key) pair costs 2 (Dqk + Dv)
     keys = 0
+    if tree is not None:   # tree verify: the prefix plus the drafts in the row's mask
+        words = tree.cpu().to(torch.int64).tolist()
+        r = 0
+        for b in range(len(p)):
+            for i in range(int(d[b])):
+                keys += int(p[b]) + bin((words[r] & 0xFFFFFFFF) & ((1 << int(d[b])) - 1)).count("1")
+                r += 1
+        flops = 2 * (wl.qk_dim + wl.v_dim) * keys * wl.num_q_heads
+        return dict(kv_call=kv_call, kv_prefix=kv_prefix, q=q_bytes, o=o_bytes, lse=lse_bytes,
+                    call_bytes=kv_call + q_bytes + o_bytes + lse_bytes,
+                    prefix_bytes=kv_prefix + q_bytes, flops=flops, rows=rows)
     for b in range(len(p)):
         for i in range(int(d[b])):
             pos = int(p[b]) + i
@@ -208,20 +219,27 @@ class ClockSampler:
 def oracle_rows_runner(pb_host: synth.Paged, window: int):
     import oracle
     wl = pb_host.wl
+    tree = synth.call_tree_masks(wl, pb_host.num_draft)
     args = (synth.raw_bits(pb_host.q), synth.raw_bits(pb_host.k_cache),
             None if wl.v_aliases_k else synth.raw_bits(pb_host.v_cache),
             pb_host.page_table.numpy(), pb_host.kv_indptr.numpy(), pb_host.seq_lens.numpy(),
             pb_host.num_draft.numpy())
     kw = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim,
               v_dim=wl.v_dim, page_size=pb_host.page_size, dtype=synth.DTYPE_CODES[wl.dtype],
-              scale=wl.scale, window=window, v_aliases_k=wl.v_aliases_k)
+              scale=wl.scale, window=window, v_aliases_k=wl.v_aliases_k,
+              tree_mask=None if tree is None else tree.numpy().astype(np.int64) & 0xFFFFFFFF)
     p = pb_host.seq_lens.numpy().astype(np.int64)
     d = pb_host.num_draft.numpy().astype(np.int64)
+    words = None if tree is None else (tree.numpy().astype(np.int64) & 0xFFFFFFFF).tolist()
     rows, keys = [], []
+    qr = 0
     for b in range(len(p)):
         for i in range(int(d[b])):
             pos = int(p[b]) + i
             k = pos + 1 - (max(0, pos - window) if window >= 0 else 0)
+            if words is not None:
+                k = int(p[b]) + bin(words[qr] & ((1 << int(d[b])) - 1)).count("1")
+            qr += 1
             for h in range(wl.num_q_heads):
                 rows.append((b, i, h))
                 keys.append(k)
@@ -333,14 +351,16 @@ def ours_arm(args):
     lse = torch.empty(pb.total_q, wl.num_q_heads, dtype=torch.float32, device=dev)
     vcache = None if wl.v_aliases_k else pb.v_cache
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    acct = call_accounting(pb, window)
+    tree = synth.call_tree_masks(wl, pb.num_draft.cpu())
+    tree = None if tree is None else tree.to(dev)
+    acct = call_accounting(pb, window, tree)
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
 
     def call(events=None, q=pb.q, pt=pb.page_table, ip=pb.kv_indptr, sl=pb.seq_lens,
-             nd=pb.num_draft, o=out, l=lse):
+             nd=pb.num_draft, o=out, l=lse, tm=tree):
         attn(q, pb.k_cache, vcache, pt, ip, sl, nd, page_size=pb.page_size, scale=wl.scale,
-             window=window, out=o, lse=l, stream=stream, events=events)
+             window=window, out=o, lse=l, stream=stream, events=events, tree_mask=tm)
 
     for _ in range(warmup):
         flush.zero_()
@@ -401,6 +421,8 @@ def ours_arm(args):
         d_q, d_pt, d_ip, d_sl, d_nd = (torch.empty_like(pb.q), torch.empty_like(pb.page_table),
                                        torch.empty_like(pb.kv_indptr), torch.empty_like(pb.seq_lens),
                                        torch.empty_like(pb.num_draft))
+        h_tm = None if tree is None else pin(tree)
+        d_tm = None if tree is None else torch.empty_like(tree)
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         e2e_steps = min(steps, 1000)
@@ -411,7 +433,9 @@ def ours_arm(args):
             d_ip.copy_(h_ip, non_blocking=True)
             d_sl.copy_(h_sl, non_blocking=True)
             d_nd.copy_(h_nd, non_blocking=True)
-            call(q=d_q, pt=d_pt, ip=d_ip, sl=d_sl, nd=d_nd)
+            if d_tm is not None:
+                d_tm.copy_(h_tm, non_blocking=True)
+            call(q=d_q, pt=d_pt, ip=d_ip, sl=d_sl, nd=d_nd, tm=d_tm)
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -435,7 +459,8 @@ def ours_arm(args):
             e2e_ms = float(t.item())
         if not torch.equal(h_out, out.cpu()):
             raise RuntimeError("e2e result differs from the device result")
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_ip, h_sl, h_nd))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_ip, h_sl, h_nd)
+                  + (() if h_tm is None else (h_tm,)))
         d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
         e2e = {"value": world * e2e_steps / (e2e_ms / 1000.0), "unit": "calls/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -481,6 +506,7 @@ def ours_arm(args):
                    "page_size": pb.page_size, "num_pages": pb.num_pages, "window": window,
                    "prefix": list(wl.prefix), "draft": list(wl.draft),
                    "kv_tokens": int(lens.sum()), "num_ctas": attn.plan.num_ctas,
+                   "tree": wl.tree,
                    "l2": "flushed between steps (256 MiB write outside the timed events)"},
         "kv_gbs": kv_gbs,
         "kv_frac_of_measured_hbm": kv_gbs / hbm_peak,

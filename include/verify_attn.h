@@ -171,6 +171,33 @@ int verify_attn_paged(const va_plan *plan, int bs, const void *q, const void *k_
                       void *stream);
 
 /*
+ * Tree verify (speculative topk > 1): verify_attn_paged with a draft-token tree
+ * instead of the causal chain. The split-KV page enables its kernel only at
+ * topk = 1 and leaves topk > 1 (whose baseline applies the tree's custom mask)
+ * to a follow-up; this is that follow-up on the same split-KV path.
+ *
+ *   tree_mask   int32 [sum_b D_b], one word per query row (rows ordered as in
+ *               q): bit d of row i's word set means draft row i attends to
+ *               draft token d of its sequence (an EAGLE tree row sets the bits
+ *               of its ancestors and of itself); bits >= D_b are ignored.
+ * Every row sees the whole prefix 0 .. P_b - 1; the drafts keep their logical
+ * positions P_b .. P_b + D_b - 1 in the page table (as at topk = 1). There is
+ * no window argument: a sliding window is not defined for tree rows here. A
+ * row that sees no key at all (an empty prefix and no bit set) gets zeros and
+ * lse = -inf. A chain mask (row i sets bits 0 .. i) reproduces
+ * verify_attn_paged.
+ * events is NULL, or four CUDA events recorded as in
+ * verify_attn_paged_profiled. Other arguments, layouts, ownership and status
+ * codes are those of verify_attn_paged; tree_mask == NULL returns
+ * VA_INVALID_ARG.
+ */
+int verify_attn_paged_tree(const va_plan *plan, int bs, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *page_table, const int32_t *kv_indptr,
+                           const int32_t *seq_lens, const int32_t *num_draft,
+                           const int32_t *tree_mask, int page_size, float scale, void *out,
+                           float *lse, void *workspace, void *stream, void *const events[4]);
+
+/*
  * verify_attn_paged, plus four CUDA events (cudaEvent_t, created by the caller)
  * recorded on the stream: before the work-list kernel, before the prefix
  * kernel, before the combine kernel, and after it. For profiling only.

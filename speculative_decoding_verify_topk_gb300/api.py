@@ -48,8 +48,10 @@ class VerifyAttention:
 
     def __call__(self, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft, *,
                  page_size: int, scale: float, window: int = -1, out=None, lse=None,
-                 stream=None, events=None):
-        """Runs verify attention; returns (out [sum D_b, Hq, v_dim], lse [sum D_b, Hq])."""
+                 stream=None, events=None, tree_mask=None):
+        """Runs verify attention; returns (out [sum D_b, Hq, v_dim], lse [sum D_b, Hq]).
+        tree_mask (int32 [sum D_b], tree verify at topk > 1): bit d of row i's
+        word lets the row see draft d; window must stay -1."""
         total_q = q.shape[0]
         if out is None:
             out = torch.empty(total_q, self.num_q_heads, self.v_dim, dtype=self.dtype,
@@ -63,6 +65,15 @@ class VerifyAttention:
                         ("seq_lens", seq_lens), ("num_draft", num_draft)):
             if t.dtype != torch.int32 or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous int32 tensor")
+        if tree_mask is not None:
+            if window >= 0:
+                raise ValueError("tree verify takes no window")
+            if tree_mask.dtype != torch.int32 or not tree_mask.is_contiguous():
+                raise ValueError("tree_mask must be a contiguous int32 tensor")
+            binding.verify_attn_paged_tree(self.plan, seq_lens.shape[0], q, k_cache, v_cache, page_table,
+                                           kv_indptr, seq_lens, num_draft, tree_mask, page_size, scale,
+                                           out, lse, self.workspace, stream=stream, events=events)
+            return out, lse
         binding.verify_attn_paged(self.plan, seq_lens.shape[0], q, k_cache, v_cache, page_table,
                                   kv_indptr, seq_lens, num_draft, page_size, scale, window, out,
                                   lse, self.workspace, stream=stream, events=events)

@@ -20,7 +20,8 @@ VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
-           "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table")
+           "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table",
+           "verify_attn_paged_tree")
 
 
 class Problem(ctypes.Structure):
@@ -88,6 +89,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.verify_attn_last_error.restype = ctypes.c_char_p
         lib.verify_attn_launches_per_call.argtypes = [ctypes.POINTER(Plan)]
         lib.verify_attn_launches_per_call.restype = I
+        lib.verify_attn_paged_tree.argtypes = [ctypes.POINTER(Plan), I, P, P, P, P, P, P, P, P, I,
+                                               ctypes.c_float, P, P, P, P, ctypes.POINTER(ctypes.c_void_p)]
+        lib.verify_attn_paged_tree.restype = I
         L = ctypes.c_int64
         lib.verify_attn_build_page_table.argtypes = [I, I, L, P, P, P, P, P, L, I, P, P, P]
         lib.verify_attn_build_page_table.restype = I
@@ -177,3 +181,25 @@ def verify_attn_build_page_table(bs: int, page_size: int, num_pages: int, kv_ind
         _ptr(error_word), _stream_handle(stream))
     if rc != VA_OK:
         raise VerifyAttnError(rc, "verify_attn_build_page_table")
+
+
+def verify_attn_paged_tree(plan: Plan, bs: int, q, k_cache, v_cache, page_table, kv_indptr, seq_lens,
+                           num_draft, tree_mask, page_size: int, scale: float, out, lse, workspace,
+                           stream=None, events=None) -> None:
+    """Calls verify_attn_paged_tree (tree verify: tree_mask int32 [sum D_b], bit
+    d of row i's word = the row sees draft d; optional four torch.cuda.Event
+    objects as in the profiled call); raises VerifyAttnError on a nonzero status."""
+    ev = None
+    if events is not None:
+        handles = []
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+                e.record()
+            handles.append(e.cuda_event)
+        ev = (ctypes.c_void_p * 4)(*handles)
+    rc = load_library().verify_attn_paged_tree(
+        ctypes.byref(plan), int(bs), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+        _ptr(kv_indptr), _ptr(seq_lens), _ptr(num_draft), _ptr(tree_mask), int(page_size), float(scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), _stream_handle(stream), ev)
+    if rc != VA_OK:
+        raise VerifyAttnError(rc, "verify_attn_paged_tree")

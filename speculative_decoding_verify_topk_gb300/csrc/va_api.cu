@@ -208,8 +208,9 @@ namespace va {
 int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
         const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
-        void* workspace, void* stream, void* const* events) {
+        void* workspace, void* stream, void* const* events, const int32_t* tree_mask) {
     if (!plan) return VA_INVALID_ARG;
+    if (tree_mask && (window >= 0 || !is_aligned(tree_mask, 4))) return VA_INVALID_ARG;
     const va_problem& p = plan->problem;
     if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_MLA || plan->num_ctas < 1 ||
         plan->rows_cap < 1 || plan->workspace_bytes == 0 || plan->tile_tokens < 1)
@@ -238,6 +239,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.kv_indptr = kv_indptr;
     a.seq_lens = seq_lens;
     a.num_draft = num_draft;
+    a.tree = reinterpret_cast<const uint32_t*>(tree_mask);
     a.out = out;
     a.lse = lse;
     a.header = reinterpret_cast<int32_t*>(ws);
@@ -324,6 +326,17 @@ extern "C" int verify_attn_paged(const va_plan* plan, int bs, const void* q, con
                                  void* out, float* lse, void* workspace, void* stream) {
     return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
                    page_size, scale, window, out, lse, workspace, stream, nullptr);
+}
+
+extern "C" int verify_attn_paged_tree(const va_plan* plan, int bs, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* page_table,
+                                      const int32_t* kv_indptr, const int32_t* seq_lens,
+                                      const int32_t* num_draft, const int32_t* tree_mask, int page_size,
+                                      float scale, void* out, float* lse, void* workspace, void* stream,
+                                      void* const events[4]) {
+    if (!tree_mask) return VA_INVALID_ARG;
+    return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft, page_size,
+                   scale, -1, out, lse, workspace, stream, events, tree_mask);
 }
 
 extern "C" int verify_attn_paged_profiled(const va_plan* plan, int bs, const void* q,

@@ -61,6 +61,7 @@ struct Args {
     const int32_t* kv_indptr;
     const int32_t* seq_lens;
     const int32_t* num_draft;
+    const uint32_t* tree;    // tree verify: bit d of tree[qoff + i] = row i sees draft d; nullptr: causal
     void* out;
     float* lse;
     int32_t* header;         // workspace header words
@@ -86,7 +87,7 @@ struct Args {
 int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
         const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
-        void* workspace, void* stream, void* const* events);
+        void* workspace, void* stream, void* const* events, const int32_t* tree_mask = nullptr);
 
 // Launches `kern` with programmatic stream serialization: it may begin while
 // the preceding kernel on the stream finishes, and must call pdl_wait()

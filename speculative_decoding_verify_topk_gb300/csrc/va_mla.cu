@@ -426,11 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(b_qtmem);
                 }
-                const int hi = si.prefix + i;
+                // causal: keys up to P + i; tree verify: every prefix key and
+                // the drafts in the row block's mask (one draft per block)
+                const int hi = a.tree ? si.prefix + si.draft - 1 : si.prefix + i;
                 const int lo = max(si.lo, a.window >= 0 ? si.prefix + i - a.window : 0);
                 const int j0 = si.a0 + cur.t * kTok;
                 const int seq_end = si.prefix + si.draft;
                 const bool live_rows = i < si.draft;
+                const uint32_t tm = (a.tree && live_rows) ? __ldg(a.tree + si.qoff + i) : 0u;
 
                 // 1. scores from TMEM
                 wait_or_abort(b_sfull, k & 1, 7);
@@ -451,11 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(b_sfree);
                 // 2. mask (the same for every row of the block) and online softmax
                 //    in base 2 with lazy rescaling by 2^8
-                if (!live_rows || j0 < lo || j0 + kTok - 1 > hi) {
+                if (!live_rows || j0 < lo || j0 + kTok - 1 > hi || (a.tree && j0 + kTok > si.prefix)) {
 #pragma unroll
                     for (int j = 0; j < kTok; ++j) {
                         const int t = j0 + j;
-                        if (!live_rows || t > hi || t < lo) s[j] = -INFINITY;
+                        if (!live_rows || t > hi || t < lo ||
+                            (a.tree && t >= si.prefix && !((tm >> (t - si.prefix)) & 1u)))
+                            s[j] = -INFINITY;
                     }
                 }
                 float mx[4] = {s[0], s[1], s[2], s[3]};

@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
         for (int r = warp; r < rows_b; r += kWarps) {
             const int i = r / a.group;
             const int lo_r = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
-            const int hi_r = si.prefix + i;   // causal: drafts 0 .. i
+            // causal: drafts 0 .. i; tree verify: the drafts set in the row's mask
+            const int hi_r = a.tree ? si.prefix + si.draft - 1 : si.prefix + i;
+            const uint32_t tm = a.tree ? __ldg(a.tree + si.qoff + i) : 0u;
             float sc[2];
             for (int h = 0; h < 2; ++h) {
                 const int t = lane + 32 * h;
@@ -134,7 +136,9 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
                     acc = fmaf(x.z, y.z, acc);
                     acc = fmaf(x.w, y.w, acc);
                 }
-                sc[h] = (j > hi_r || j < lo_r || j < si.lo) ? -INFINITY : acc * a.scale_log2;
+                const bool hidden = j > hi_r || j < lo_r || j < si.lo ||
+                                    (a.tree && j >= si.prefix && !((tm >> (j - si.prefix)) & 1u));
+                sc[h] = hidden ? -INFINITY : acc * a.scale_log2;
             }
             float mx = fmaxf(sc[0], sc[1]);
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));

@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[DV / 8][4];
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         int rows_b = 0, lo_r[2] = {0, 0}, hi_r[2] = {0, 0};
+        uint32_t tm_r[2] = {0u, 0u};   // tree verify: the rows' draft masks
         SeqInfo si = {};
         auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
             if (*(volatile int*)&abort_flag) return;
@@ -290,7 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int r = wm * 16 + (lane >> 2) + 8 * h;
                     const int i = r / a.group;
                     lo_r[h] = a.window >= 0 ? si.prefix + i - a.window : -0x7fffffff;
-                    hi_r[h] = r < rows_b ? si.prefix + i : -0x7fffffff;   // padding rows see nothing
+                    // tree verify: every prefix key, and the drafts in the row's mask
+                    hi_r[h] = r < rows_b ? (a.tree ? si.prefix + si.draft - 1 : si.prefix + i)
+                                         : -0x7fffffff;   // padding rows see nothing
+                    tm_r[h] = (a.tree && r < rows_b) ? __ldg(a.tree + si.qoff + i) : 0u;
                 }
             }
             wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
@@ -339,7 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v = s[n][e] * a.scale_log2;
                     if (need_mask) {
                         const int j = j_base + n * 8 + (e & 1);
-                        if (j > hi_r[e >> 1] || j < lo_r[e >> 1]) v = -INFINITY;
+                        if (j > hi_r[e >> 1] || j < lo_r[e >> 1] ||
+                            (a.tree && j >= si.prefix && !((tm_r[e >> 1] >> (j - si.prefix)) & 1u)))
+                            v = -INFINITY;
                     }
                     s[n][e] = v;
                     mx[e >> 1] = fmaxf(mx[e >> 1], v);

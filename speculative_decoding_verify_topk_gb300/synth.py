@@ -54,6 +54,7 @@ class Workload:
     v_aliases_k: bool = False
     pool_tokens: int | None = None   # None: 1.25x the pages needed
     window: tuple = (-1,)            # window of call c is window[c % len(window)]
+    tree: str | None = None          # tree verify (topk > 1): draft_trees shape, None = causal
 
     @property
     def group(self) -> int:
@@ -87,7 +88,19 @@ WORKLOADS = {
     "draft_extend": Workload("draft_extend", torch.bfloat16, 64, 32, 8, 128, 128, 16,
                              ("uniform", 1024, 8192), ("choice", [1, 2, 3, 4, 5]), 5,
                              1.0 / math.sqrt(128)),
+    # tree verify at topk > 1: the Llama-3.1-8B-shaped batch with 8 draft tokens
+    # per sequence forming a random tree (each row sees its ancestors)
+    "llama8b_tree": Workload("llama8b_tree", torch.bfloat16, 16, 32, 8, 128, 128, 4,
+                             ("uniform", 1024, 8192), ("fixed", 8), 6, 1.0 / math.sqrt(128),
+                             pool_tokens=1 << 21, tree="random"),
 }
+
+
+def call_tree_masks(wl: Workload, num_draft):
+    """The tree_mask input of a tree-verify workload (None for a causal one)."""
+    if wl.tree is None:
+        return None
+    return tree_masks(draft_trees([int(x) for x in num_draft], seed=wl.seed, shape=wl.tree))
 
 
 @dataclasses.dataclass
