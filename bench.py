@@ -326,6 +326,29 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (a timed region's length): the job takes
+    as long as its slowest replica. One process group per job (NCCL on the GPU
+    box, gloo in the CPU tests); identity for a single rank."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, total_ms: float) -> float:
+    """Whole-job calls/s: every replica runs `steps` calls of its own batch
+    (weak scaling), all within the max-over-ranks time total_ms."""
+    return world * steps / (total_ms / 1000.0)
+
+
+def replica_seed(wl, rank: int) -> int:
+    """Each rank's replica draws its own batch of the workload's shape."""
+    return wl.seed + 1000 * rank
+
+
 def ours_arm(args):
     import speculative_decoding_verify_topk_gb300 as va
     world, rank, local = dist_env()
@@ -339,7 +362,7 @@ def ours_arm(args):
     if args.compact_pool:
         wl = wl.replace(pool_tokens=None)
     window = wl.window_for_call(0)
-    pb = synth.make_batch(wl, device=dev, seed=wl.seed + 1000 * rank)
+    pb = synth.make_batch(wl, device=dev, seed=replica_seed(wl, rank))
     lens = pb.seq_lens.long() + pb.num_draft.long()
     attn = va.VerifyAttention(max_bs=wl.bs, max_draft=int(pb.num_draft.max()),
                               num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
@@ -404,13 +427,9 @@ def ours_arm(args):
     combine_ms = [e[2].elapsed_time(e[3]) for e in evs]
     worklist_ms = [e[0].elapsed_time(e[1]) for e in evs]
     profiled_step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / steps
-    value = world * steps / (total_ms / 1000.0)
+    value = job_rate(world, steps, total_ms)
 
     # ---- end to end through host buffers
     e2e = None
@@ -452,17 +471,13 @@ def ours_arm(args):
             b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         if not torch.equal(h_out, out.cpu()):
             raise RuntimeError("e2e result differs from the device result")
         h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_ip, h_sl, h_nd)
                   + (() if h_tm is None else (h_tm,)))
         d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
-        e2e = {"value": world * e2e_steps / (e2e_ms / 1000.0), "unit": "calls/s",
+        e2e = {"value": job_rate(world, e2e_steps, e2e_ms), "unit": "calls/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / e2e_steps}
 
