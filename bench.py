@@ -227,6 +227,7 @@ def oracle_rows_runner(pb_host: synth.Paged, window: int):
     kw = dict(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim,
               v_dim=wl.v_dim, page_size=pb_host.page_size, dtype=synth.DTYPE_CODES[wl.dtype],
               scale=wl.scale, window=window, v_aliases_k=wl.v_aliases_k,
+              kv_dtype=synth.DTYPE_CODES[wl.kv_type], k_scale=wl.k_scale, v_scale=wl.v_scale,
               tree_mask=None if tree is None else tree.numpy().astype(np.int64) & 0xFFFFFFFF)
     p = pb_host.seq_lens.numpy().astype(np.int64)
     d = pb_host.num_draft.numpy().astype(np.int64)

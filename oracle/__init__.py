@@ -35,7 +35,7 @@ _SRC = os.path.join(_HERE, "verify_attn_oracle.c")
 _LOCK = threading.Lock()
 _LIBS: dict[int, ctypes.CDLL] = {}
 
-DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
+DTYPE_F32, DTYPE_BF16, DTYPE_F16, DTYPE_FP8_E4M3 = 0, 1, 2, 3
 _ERRORS = {
     1: "invalid argument",
     2: "page id outside the pool",
@@ -72,10 +72,13 @@ def _lib(mutant: int = 0, out_dir: str | None = None) -> ctypes.CDLL:
             f = lib.oracle_verify_attn
             f.restype = ctypes.c_int
             P = ctypes.c_void_p
-            f.argtypes = [ctypes.c_int] * 7 + [P, P, P, ctypes.c_int, P, P, ctypes.c_int64,
+            f.argtypes = [ctypes.c_int] * 8 + [ctypes.c_double, ctypes.c_double,
+                                               P, P, P, ctypes.c_int, P, P, ctypes.c_int64,
                                                P, P, ctypes.c_double, ctypes.c_int, P, ctypes.c_int,
                                                P, ctypes.c_int64, P, P, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_decode_e4m3.argtypes = [ctypes.c_int]
+            lib.oracle_decode_e4m3.restype = ctypes.c_double
             lib.oracle_mutant_id.restype = ctypes.c_int
             _LIBS[key] = lib
         return _LIBS[key]
@@ -86,8 +89,13 @@ def max_threads() -> int:
 
 
 def _as_raw(a: np.ndarray, dtype_code: int) -> np.ndarray:
-    """Arrays reach C as their raw element bits: float32, or uint16 for bf16/fp16."""
+    """Arrays reach C as their raw element bits: float32, uint16 for bf16/fp16,
+    uint8 for FP8 E4M3."""
     a = np.ascontiguousarray(a)
+    if dtype_code == DTYPE_FP8_E4M3:
+        if a.dtype not in (np.uint8, np.int8):
+            raise TypeError("FP8 oracle inputs must be their uint8 bit patterns")
+        return a.view(np.uint8)
     if dtype_code == DTYPE_F32:
         if a.dtype != np.float32:
             raise TypeError("fp32 oracle inputs must be float32 arrays")
@@ -107,7 +115,7 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
                 dtype: int, scale: float, window: int = -1, v_aliases_k: bool = False,
                 num_pages: int | None = None, num_splits: int = 1, rows=None,
                 threads: int = 0, mutant: int = 0, mutant_dir: str | None = None,
-                tree_mask=None):
+                tree_mask=None, kv_dtype: int = -1, k_scale: float = 1.0, v_scale: float = 1.0):
     """Verify attention in fp64.
 
     Arguments follow the C entry point ``verify_attn_paged`` (same meaning and
@@ -115,6 +123,9 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
     v_cache [pages, page_size, Hkv, Dv] (ignored when ``v_aliases_k``);
     page_table / kv_indptr CSR over pages; seq_lens = prefix lengths P_b;
     num_draft = D_b. 16-bit inputs are passed as their bit patterns (uint16).
+
+    ``kv_dtype`` (-1: same as ``dtype``; 3: FP8 E4M3 pools passed as uint8 bit
+    patterns) with ``k_scale`` / ``v_scale``: K = k_scale * stored, V = v_scale * stored.
 
     ``tree_mask`` (tree verify, topk > 1): None for causal rows, else uint32
     [sum D_b]; bit d of row i's word means the row sees draft d (every prefix
@@ -127,8 +138,9 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
     """
     lib = _lib(mutant, mutant_dir)
     q = _as_raw(q, dtype)
-    k_cache = _as_raw(k_cache, dtype)
-    v_cache = k_cache if v_aliases_k else _as_raw(v_cache, dtype)
+    kvd = dtype if kv_dtype < 0 else kv_dtype
+    k_cache = _as_raw(k_cache, kvd)
+    v_cache = k_cache if v_aliases_k else _as_raw(v_cache, kvd)
     page_table, kv_indptr = _i32(page_table), _i32(kv_indptr)
     seq_lens, num_draft = _i32(seq_lens), _i32(num_draft)
     bs = int(seq_lens.shape[0])
@@ -155,7 +167,7 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
             raise ValueError("tree_mask needs one word per query row")
     ptr = lambda a: None if a is None else a.ctypes.data
     rc = lib.oracle_verify_attn(bs, num_q_heads, num_kv_heads, qk_dim, v_dim, page_size, dtype,
-                                ptr(q), ptr(k_cache), ptr(v_cache), int(bool(v_aliases_k)),
+                                int(kv_dtype), float(k_scale), float(v_scale), ptr(q), ptr(k_cache), ptr(v_cache), int(bool(v_aliases_k)),
                                 ptr(page_table), ptr(kv_indptr), int(num_pages),
                                 ptr(seq_lens), ptr(num_draft), float(scale), int(window),
                                 ptr(tree_mask), int(num_splits), ptr(rows_arr), int(n_rows),
@@ -163,3 +175,8 @@ def verify_attn(q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
     if rc != 0:
         raise ValueError(f"oracle rejected its input: {_ERRORS.get(rc, rc)}")
     return out, lse
+
+
+def decode_e4m3(code: int) -> float:
+    """The oracle's FP8 E4M3 decoder (for its pin)."""
+    return _lib(0, None).oracle_decode_e4m3(int(code))

@@ -34,6 +34,11 @@
  *    page_table[kv_indptr[b] + k].
  *  - lse is the natural logarithm of sum_j exp(scale * q . k_j).
  *  - Absorbed MLA (v_aliases_k): V is the first Dv entries of the K row.
+ *  - FP8 KV ("Split-KV flash-decode attention for EAGLE target-verify (Triton
+ *    backend)", Modifications: the prefix stage applies the fp8 k_scale /
+ *    v_scale dequant multipliers as the extend kernel does): pools stored as
+ *    FP8 E4M3 hold K / scale and V / scale per tensor; K = k_scale * stored,
+ *    V = v_scale * stored, and q stays in its 16-bit type.
  *  - Tree verify (topk > 1, the follow-up the split-KV page defers; its
  *    baseline applies the tree's custom mask): when tree_mask is given, row i
  *    of sequence b sees every prefix key 0 .. P_b - 1 and the draft key
@@ -73,7 +78,7 @@
 #define ORACLE_MUTANT 0
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_FP8_E4M3 = 3 };
 
 enum {
     ORACLE_OK = 0,
@@ -108,19 +113,43 @@ static double decode_bf16(uint16_t h)
     return (double)f;
 }
 
+/*
+ * FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits,
+ * no infinities; exponent 15 with fraction 7 is NaN, every other pattern is a
+ * number (so the largest is 1.75 * 2^8 = 448).
+ */
+static double decode_e4m3(uint8_t x)
+{
+    int sign = (x >> 7) & 1;
+    int expo = (x >> 3) & 0xf;
+    int frac = x & 0x7;
+    double mag;
+    if (expo == 15 && frac == 7)
+        mag = NAN;
+    else if (expo == 0)
+        mag = ldexp((double)frac, -9);                  /* subnormal: frac/8 * 2^-6 */
+    else
+        mag = ldexp((double)(frac | 0x8), expo - 10);   /* (1.frac) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* Exported for the decoder pin (all 256 codes against an independent decoder). */
+double oracle_decode_e4m3(int x) { return decode_e4m3((uint8_t)x); }
+
 static double elem(const void *base, int dtype, int64_t idx)
 {
     switch (dtype) {
     case ORACLE_F32: return (double)((const float *)base)[idx];
     case ORACLE_BF16: return decode_bf16(((const uint16_t *)base)[idx]);
+    case ORACLE_FP8_E4M3: return decode_e4m3(((const uint8_t *)base)[idx]);
     default: return decode_f16(((const uint16_t *)base)[idx]);
     }
 }
 
 typedef struct {
-    int bs, hq, hkv, dqk, dv, page_size, dtype, v_aliases_k, window, num_splits;
+    int bs, hq, hkv, dqk, dv, page_size, dtype, kv_dtype, v_aliases_k, window, num_splits;
     int64_t num_pages;
-    double scale;
+    double scale, k_scale, v_scale;
     const void *q, *k, *v;
     const int32_t *page_table, *kv_indptr, *seq_lens, *num_draft;
     const uint32_t *tree_mask;   /* NULL: causal */
@@ -147,19 +176,25 @@ static int kv_head_of(const problem *pb, int h)
 #endif
 }
 
+/* Dequantised K / V elements: the stored value times the per-tensor scale. */
 static double key_elem(const problem *pb, int64_t slot, int g, int d)
 {
-    return elem(pb->k, pb->dtype, (slot * pb->hkv + g) * pb->dqk + d);
+    return pb->k_scale * elem(pb->k, pb->kv_dtype, (slot * pb->hkv + g) * pb->dqk + d);
 }
 
 static double value_elem(const problem *pb, int64_t slot, int g, int d)
 {
-    if (pb->v_aliases_k)
-        return elem(pb->k, pb->dtype, (slot * pb->hkv + g) * pb->dqk + d);
-#if ORACLE_MUTANT == 9
-    return elem(pb->k, pb->dtype, (slot * pb->hkv + g) * pb->dqk + d); /* planted: V read from K */
+#if ORACLE_MUTANT == 12
+    const double vs = 1.0; /* planted: the V scale dropped */
 #else
-    return elem(pb->v, pb->dtype, (slot * pb->hkv + g) * pb->dv + d);
+    const double vs = pb->v_scale;
+#endif
+    if (pb->v_aliases_k)
+        return vs * elem(pb->k, pb->kv_dtype, (slot * pb->hkv + g) * pb->dqk + d);
+#if ORACLE_MUTANT == 9
+    return vs * elem(pb->k, pb->kv_dtype, (slot * pb->hkv + g) * pb->dqk + d); /* planted: V read from K */
+#else
+    return vs * elem(pb->v, pb->kv_dtype, (slot * pb->hkv + g) * pb->dv + d);
 #endif
 }
 
@@ -327,7 +362,12 @@ static int check_tables(const problem *pb)
  *   v_cache     [num_pages, page_size, hkv, dv]   (ignored when v_aliases_k)
  *   page_table  int32, CSR over pages; kv_indptr int32 [bs + 1]
  *   seq_lens    int32 [bs] prefix lengths; num_draft int32 [bs]
- *   dtype       0 fp32, 1 bf16, 2 fp16 (q, k_cache and v_cache share it)
+ *   dtype       0 fp32, 1 bf16, 2 fp16: q (and k_cache / v_cache unless kv_dtype says
+ *               otherwise)
+ *   kv_dtype    -1: same as dtype; 3: FP8 E4M3 pools (bytes)
+ *   k_scale, v_scale  per-tensor dequantisation scales: K = k_scale * stored,
+ *               V = v_scale * stored (1.0 for unquantised pools); the split-KV page
+ *               applies them in the prefix stage exactly as the extend kernel does
  *   window      < 0: no window (required with tree_mask)
  *   tree_mask   NULL: causal rows; else uint32 [sum D_b], bit d of row i's word:
  *               the row sees draft d (tree verify)
@@ -338,6 +378,7 @@ static int check_tables(const problem *pb)
  * Returns 0 on success, otherwise an ORACLE_ code and writes nothing useful.
  */
 int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, int dtype,
+                       int kv_dtype, double k_scale, double v_scale,
                        const void *q, const void *k_cache, const void *v_cache, int v_aliases_k,
                        const int32_t *page_table, const int32_t *kv_indptr, int64_t num_pages,
                        const int32_t *seq_lens, const int32_t *num_draft, double scale, int window,
@@ -352,12 +393,15 @@ int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, 
     if (bs < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || dqk <= 0 || dv <= 0 || page_size <= 0)
         return ORACLE_BAD_ARG;
     if (dtype < ORACLE_F32 || dtype > ORACLE_F16) return ORACLE_BAD_ARG;
+    if (kv_dtype < 0) kv_dtype = dtype;
+    if (kv_dtype < ORACLE_F32 || kv_dtype > ORACLE_FP8_E4M3) return ORACLE_BAD_ARG;
     if (v_aliases_k && dv > dqk) return ORACLE_BAD_ARG;
     if (tree_mask && window >= 0) return ORACLE_BAD_ARG;
     if (bs == 0) return ORACLE_OK;
 
     pb.bs = bs; pb.hq = hq; pb.hkv = hkv; pb.dqk = dqk; pb.dv = dv;
     pb.page_size = page_size; pb.dtype = dtype; pb.v_aliases_k = v_aliases_k;
+    pb.kv_dtype = kv_dtype; pb.k_scale = k_scale; pb.v_scale = v_scale;
     pb.window = window; pb.num_splits = num_splits; pb.num_pages = num_pages;
     pb.scale = scale; pb.q = q; pb.k = k_cache; pb.v = v_cache;
     pb.page_table = page_table; pb.kv_indptr = kv_indptr;

@@ -55,6 +55,13 @@ class Workload:
     pool_tokens: int | None = None   # None: 1.25x the pages needed
     window: tuple = (-1,)            # window of call c is window[c % len(window)]
     tree: str | None = None          # tree verify (topk > 1): draft_trees shape, None = causal
+    kv_dtype: torch.dtype | None = None   # K/V pool element type (None: dtype); float8_e4m3fn
+    k_scale: float = 1.0             # per-tensor dequantisation scales: K = k_scale * stored
+    v_scale: float = 1.0
+
+    @property
+    def kv_type(self) -> torch.dtype:
+        return self.dtype if self.kv_dtype is None else self.kv_dtype
 
     @property
     def group(self) -> int:
@@ -192,8 +199,11 @@ def make_logical(wl: Workload, device="cpu", seed: int | None = None,
     g = _gen(seed + 7919, device)
     f32 = dict(dtype=torch.float32, device=device, generator=g)
     q = torch.randn(total_q, wl.num_q_heads, wl.qk_dim, **f32).to(wl.dtype)
-    k = torch.randn(total_t, wl.num_kv_heads, wl.qk_dim, **f32).to(wl.dtype)
-    v = None if wl.v_aliases_k else torch.randn(total_t, wl.num_kv_heads, wl.v_dim, **f32).to(wl.dtype)
+    # K/V ~ N(0, 1) stored as value / scale in the pool type (a per-tensor
+    # quantised cache when kv_dtype is FP8)
+    k = (torch.randn(total_t, wl.num_kv_heads, wl.qk_dim, **f32) / wl.k_scale).to(wl.kv_type)
+    v = None if wl.v_aliases_k else \
+        (torch.randn(total_t, wl.num_kv_heads, wl.v_dim, **f32) / wl.v_scale).to(wl.kv_type)
     return Logical(wl, seq_lens, num_draft, q, k, v, tok_off)
 
 
@@ -234,13 +244,19 @@ def paginate(lg: Logical, page_size: int | None = None, pool_pages: int | None =
     slots = slots.to(device)
 
     hkv = wl.num_kv_heads
-    k_cache = torch.full((pool_pages, ps, hkv, wl.qk_dim), float("nan"), dtype=wl.dtype, device=device)
-    k_cache.view(-1, hkv, wl.qk_dim).index_copy_(0, slots, lg.k.to(device))
+    kvt = wl.kv_type
+
+    def scatter(pool, rows):   # through an integer view: index_copy_ lacks FP8 kernels
+        iv = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[pool.element_size()]
+        pool.view(iv).view(-1, *rows.shape[1:]).index_copy_(0, slots, rows.to(device).view(iv))
+
+    k_cache = torch.full((pool_pages, ps, hkv, wl.qk_dim), float("nan"), dtype=kvt, device=device)
+    scatter(k_cache, lg.k)
     if wl.v_aliases_k:
         v_cache = k_cache
     else:
-        v_cache = torch.full((pool_pages, ps, hkv, wl.v_dim), float("nan"), dtype=wl.dtype, device=device)
-        v_cache.view(-1, hkv, wl.v_dim).index_copy_(0, slots, lg.v.to(device))
+        v_cache = torch.full((pool_pages, ps, hkv, wl.v_dim), float("nan"), dtype=kvt, device=device)
+        scatter(v_cache, lg.v)
     return Paged(wl, lg.q.to(device), k_cache, v_cache, page_table.to(device), kv_indptr.to(device),
                  lg.seq_lens.to(device), lg.num_draft.to(device), ps)
 
@@ -314,15 +330,17 @@ def raw_bits(t: torch.Tensor):
         return t.numpy()
     if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     raise TypeError(t.dtype)
 
 
-DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.float8_e4m3fn: 3}
 
 
 def kv_token_bytes(wl: Workload) -> int:
     """Bytes of K (+ V unless aliased) that one KV token carries across all kv-heads."""
-    e = torch.finfo(wl.dtype).bits // 8
+    e = torch.finfo(wl.kv_type).bits // 8
     return wl.num_kv_heads * (wl.qk_dim + (0 if wl.v_aliases_k else wl.v_dim)) * e
 
 

@@ -239,9 +239,52 @@ def pin_tree_split_invariance(m=0, d=None):
         _close(lse, base[1], 1e-12, f"tree lse S={s}")
 
 
+FP8_WL = dict(kv_dtype=torch.float8_e4m3fn, k_scale=0.75, v_scale=1.375)
+
+
+def pin_fp8_brute_force(m=0, d=None):
+    """FP8 E4M3 pools with per-tensor scales: the oracle against dense attention
+    over K/V dequantised by torch's own FP8 conversion."""
+    for dtype in (torch.bfloat16, torch.float16):
+        lg, pb = _pin_batch(dtype, **FP8_WL)
+        for window in (-1, 5):
+            out, lse = oracle_on(pb, window=window, mutant=m, mutant_dir=d)
+            bo, bl = brute_force(lg, window=window)
+            _close(out, bo, 1e-12, f"fp8 out {dtype} W={window}")
+            _close(lse, bl, 1e-12, f"fp8 lse {dtype} W={window}")
+
+
+def pin_fp8_scales(m=0, d=None):
+    """v_scale scales the output and leaves lse alone (a power of two exactly);
+    k_scale is the softmax scale times k_scale."""
+    lg, pb = _pin_batch(torch.bfloat16, **FP8_WL)
+    wl = pb.wl
+    base_o, base_l = oracle_on(pb, mutant=m, mutant_dir=d)
+    pb2 = synth.Paged(wl.replace(v_scale=wl.v_scale * 2), pb.q, pb.k_cache, pb.v_cache, pb.page_table,
+                      pb.kv_indptr, pb.seq_lens, pb.num_draft, pb.page_size)
+    o2, l2 = oracle_on(pb2, mutant=m, mutant_dir=d)
+    assert np.array_equal(o2, 2 * base_o) and np.array_equal(l2, base_l), "v_scale is not a pure output scale"
+    pb3 = synth.Paged(wl.replace(k_scale=1.0), pb.q, pb.k_cache, pb.v_cache, pb.page_table,
+                      pb.kv_indptr, pb.seq_lens, pb.num_draft, pb.page_size)
+    o3, l3 = oracle_on(pb3, scale=wl.scale * wl.k_scale, mutant=m, mutant_dir=d)
+    _close(o3, base_o, 1e-12, "k_scale folded into the softmax scale")
+    _close(l3, base_l, 1e-12, "k_scale folded into the softmax scale (lse)")
+
+
+def pin_fp8_decoder(m=0, d=None):
+    """All 256 E4M3 codes against torch's FP8 conversion (NaN where torch has NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    lib_dir = d
+    got = np.array([oracle._lib(m, lib_dir).oracle_decode_e4m3(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "NaN codes differ"
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)]), "E4M3 values differ"
+
+
 PINS = [pin_brute_force, pin_sdpa, pin_page_size_invariance, pin_split_invariance, pin_equal_keys,
         pin_single_key, pin_window_cases, pin_gqa_mapping, pin_mla_alias, pin_decoders,
-        pin_row_select, pin_tree_brute_force, pin_tree_chain_is_causal, pin_tree_split_invariance]
+        pin_row_select, pin_tree_brute_force, pin_tree_chain_is_causal, pin_tree_split_invariance,
+        pin_fp8_brute_force, pin_fp8_scales, pin_fp8_decoder]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -263,6 +306,7 @@ MUTANTS = {
     9: ("values read from the K pool instead of V", {"pin_brute_force", "pin_sdpa"}),
     10: ("tree mask bit index off by one", {"pin_tree_brute_force", "pin_tree_chain_is_causal"}),
     11: ("tree mask ignored (causal chain kept)", {"pin_tree_brute_force"}),
+    12: ("V dequantisation scale dropped", {"pin_fp8_brute_force", "pin_fp8_scales"}),
 }
 
 

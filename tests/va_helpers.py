@@ -20,6 +20,7 @@ def oracle_on(pb: synth.Paged, window: int = -1, num_splits: int = 1, rows=None,
         pb.seq_lens.cpu().numpy(), pb.num_draft.cpu().numpy(),
         num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim,
         v_dim=wl.v_dim, page_size=pb.page_size, dtype=synth.DTYPE_CODES[wl.dtype],
+        kv_dtype=synth.DTYPE_CODES[wl.kv_type], k_scale=wl.k_scale, v_scale=wl.v_scale,
         scale=wl.scale if scale is None else scale, window=window,
         v_aliases_k=wl.v_aliases_k, num_pages=pb.num_pages, num_splits=num_splits,
         rows=rows, threads=threads, mutant=mutant, mutant_dir=mutant_dir,
@@ -35,8 +36,9 @@ def brute_force(lg: synth.Logical, window: int = -1, scale=None, tree_parents=No
     wl = lg.wl
     scale = wl.scale if scale is None else scale
     q = lg.q.double().cpu().numpy()
-    k = lg.k.double().cpu().numpy()
-    v = (k[..., : wl.v_dim] if wl.v_aliases_k else lg.v.double().cpu().numpy())
+    k = lg.k.double().cpu().numpy() * wl.k_scale   # dequantised (scale 1 unless a quantised cache)
+    v = (k[..., : wl.v_dim] / wl.k_scale * wl.v_scale if wl.v_aliases_k
+         else lg.v.double().cpu().numpy() * wl.v_scale)
     outs, lses = [], []
     qrow = 0
     for b in range(wl.bs):
