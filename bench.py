@@ -83,11 +83,12 @@ def call_accounting(pb: synth.Paged, window: int, tree=None):
     reads the prefix part of the KV ([lo_b, P_b)) and Q; its partial results
     are overhead, not counted."""
     wl = pb.wl
-    e = torch.finfo(wl.dtype).bits // 8
+    e = torch.finfo(wl.dtype).bits // 8       # q, out
+    ekv = torch.finfo(wl.kv_type).bits // 8   # K / V pool elements
     p = pb.seq_lens.cpu().to(torch.int64)
     d = pb.num_draft.cpu().to(torch.int64)
     lo = (p - window).clamp(min=0) if window >= 0 else torch.zeros_like(p)
-    tok_bytes = wl.num_kv_heads * (wl.qk_dim + (0 if wl.v_aliases_k else wl.v_dim)) * e
+    tok_bytes = wl.num_kv_heads * (wl.qk_dim + (0 if wl.v_aliases_k else wl.v_dim)) * ekv
     kv_call = int(((p + d - lo) * tok_bytes).sum())
     kv_prefix = int(((p - lo) * tok_bytes).sum())
     rows = int(d.sum()) * wl.num_q_heads
@@ -369,7 +370,7 @@ def ours_arm(args):
                               num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
                               qk_dim=wl.qk_dim, v_dim=wl.v_dim, page_size=pb.page_size,
                               dtype=wl.dtype, max_kv_len=int(lens.max()), num_pages=pb.num_pages,
-                              v_aliases_k=wl.v_aliases_k, device=dev)
+                              v_aliases_k=wl.v_aliases_k, device=dev, kv_dtype=wl.kv_dtype)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty(pb.total_q, wl.num_q_heads, wl.v_dim, dtype=wl.dtype, device=dev)
     lse = torch.empty(pb.total_q, wl.num_q_heads, dtype=torch.float32, device=dev)
@@ -384,7 +385,8 @@ def ours_arm(args):
     def call(events=None, q=pb.q, pt=pb.page_table, ip=pb.kv_indptr, sl=pb.seq_lens,
              nd=pb.num_draft, o=out, l=lse, tm=tree):
         attn(q, pb.k_cache, vcache, pt, ip, sl, nd, page_size=pb.page_size, scale=wl.scale,
-             window=window, out=o, lse=l, stream=stream, events=events, tree_mask=tm)
+             window=window, out=o, lse=l, stream=stream, events=events, tree_mask=tm,
+             k_scale=wl.k_scale, v_scale=wl.v_scale)
 
     for _ in range(warmup):
         flush.zero_()
@@ -515,7 +517,8 @@ def ours_arm(args):
         "metric": METRIC, "value": value, "unit": "calls/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[wl.dtype],
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[wl.dtype]
+        + ("+fp8kv" if wl.kv_dtype == torch.float8_e4m3fn else ""),
         "data": "synthetic (seeded N(0,1) Q/K/V, NaN-poisoned unowned pool slots)",
         "config": {"workload": wl.name, "bs": wl.bs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "qk_dim": wl.qk_dim, "v_dim": wl.v_dim,
@@ -523,6 +526,7 @@ def ours_arm(args):
                    "prefix": list(wl.prefix), "draft": list(wl.draft),
                    "kv_tokens": int(lens.sum()), "num_ctas": attn.plan.num_ctas,
                    "tree": wl.tree,
+                   "kv_dtype": str(wl.kv_type).replace("torch.", ""),
                    "l2": "flushed between steps (256 MiB write outside the timed events)"},
         "kv_gbs": kv_gbs,
         "kv_frac_of_measured_hbm": kv_gbs / hbm_peak,

@@ -48,8 +48,9 @@ enum va_status {
     VA_DEVICE_RANGE_ERROR = 5    /* verify_attn_check only: a device-side check failed */
 };
 
-/* Element type of q, k_cache, v_cache and out. Arithmetic is fp32 throughout. */
-enum va_dtype { VA_FP32 = 0, VA_BF16 = 1, VA_FP16 = 2 };
+/* Element type of q, k_cache, v_cache and out. Arithmetic is fp32 throughout.
+ * VA_FP8_E4M3 is a K/V pool type only (va_problem.kv_dtype). */
+enum va_dtype { VA_FP32 = 0, VA_BF16 = 1, VA_FP16 = 2, VA_FP8_E4M3 = 3 };
 
 /* Which prefix kernel a plan selects. */
 enum va_path {
@@ -84,6 +85,14 @@ enum va_device_error {
  *                 prefix kernel splits the KV stream over (tests use it to
  *                 vary the split-KV partition)
  *   num_sms       0: query the current device; > 0: use this SM count
+ *   kv_dtype      0: the K/V pools have element type dtype; VA_FP8_E4M3: FP8
+ *                 E4M3 pools (one byte per element) holding K / k_scale and
+ *                 V / v_scale per tensor, the scales passed to
+ *                 verify_attn_paged_scaled ("Split-KV flash-decode attention
+ *                 for EAGLE target-verify (Triton backend)", Modifications: the
+ *                 prefix stage applies the fp8 k_scale / v_scale dequant
+ *                 multipliers). Needs dtype bf16 or fp16, separate K and V pools,
+ *                 and qk_dim, v_dim multiples of 128 (else VA_UNSUPPORTED)
  *   max_kv_len    largest P_b + D_b
  *   num_pages     pages in the K/V pools; page ids are checked against it
  */
@@ -99,7 +108,7 @@ typedef struct va_problem {
     int32_t v_aliases_k;
     int32_t num_ctas;
     int32_t num_sms;
-    int32_t reserved0;
+    int32_t kv_dtype;
     int64_t max_kv_len;
     int64_t num_pages;
 } va_problem;
@@ -169,6 +178,23 @@ int verify_attn_paged(const va_plan *plan, int bs, const void *q, const void *k_
                       const int32_t *seq_lens, const int32_t *num_draft, int page_size,
                       float scale, int window, void *out, float *lse, void *workspace,
                       void *stream);
+
+/*
+ * verify_attn_paged with per-tensor K/V dequantisation scales and an optional
+ * tree mask: K = k_scale * k_cache, V = v_scale * v_cache (an FP8 plan's pools
+ * hold K / k_scale and V / v_scale; for 16-bit pools the scales apply the
+ * same way). tree_mask is NULL (causal rows, window as in verify_attn_paged)
+ * or the tree verify mask of verify_attn_paged_tree (then window must be < 0).
+ * events is NULL or four CUDA events as in verify_attn_paged_profiled. Other
+ * arguments, layouts and status codes are those of verify_attn_paged;
+ * non-finite or non-positive scales return VA_INVALID_ARG.
+ */
+int verify_attn_paged_scaled(const va_plan *plan, int bs, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *page_table,
+                             const int32_t *kv_indptr, const int32_t *seq_lens,
+                             const int32_t *num_draft, const int32_t *tree_mask, int page_size,
+                             float scale, int window, float k_scale, float v_scale, void *out,
+                             float *lse, void *workspace, void *stream, void *const events[4]);
 
 /*
  * Tree verify (speculative topk > 1): verify_attn_paged with a draft-token tree

@@ -14,14 +14,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libverify_attn.so")
 
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_WORKSPACE_TOO_SMALL, VA_CUDA_ERROR, VA_DEVICE_RANGE_ERROR = range(6)
-VA_FP32, VA_BF16, VA_FP16 = 0, 1, 2
+VA_FP32, VA_BF16, VA_FP16, VA_FP8_E4M3 = 0, 1, 2, 3
 VA_PATH_F32, VA_PATH_MMA, VA_PATH_MLA = 1, 2, 3
 VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
            "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table",
-           "verify_attn_paged_tree")
+           "verify_attn_paged_tree", "verify_attn_paged_scaled")
 
 
 class Problem(ctypes.Structure):
@@ -31,7 +31,7 @@ class Problem(ctypes.Structure):
                 ("qk_dim", ctypes.c_int32), ("v_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("v_aliases_k", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("max_kv_len", ctypes.c_int64), ("num_pages", ctypes.c_int64)]
 
 
@@ -92,6 +92,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.verify_attn_paged_tree.argtypes = [ctypes.POINTER(Plan), I, P, P, P, P, P, P, P, P, I,
                                                ctypes.c_float, P, P, P, P, ctypes.POINTER(ctypes.c_void_p)]
         lib.verify_attn_paged_tree.restype = I
+        lib.verify_attn_paged_scaled.argtypes = [ctypes.POINTER(Plan), I, P, P, P, P, P, P, P, P, I,
+                                                 ctypes.c_float, I, ctypes.c_float, ctypes.c_float,
+                                                 P, P, P, P, ctypes.POINTER(ctypes.c_void_p)]
+        lib.verify_attn_paged_scaled.restype = I
         L = ctypes.c_int64
         lib.verify_attn_build_page_table.argtypes = [I, I, L, P, P, P, P, P, L, I, P, P, P]
         lib.verify_attn_build_page_table.restype = I
@@ -106,11 +110,11 @@ def status_string(status: int) -> str:
 def verify_attn_plan(*, max_bs: int, max_draft: int, num_q_heads: int, num_kv_heads: int,
                      qk_dim: int, v_dim: int, page_size: int, dtype: int, max_kv_len: int,
                      num_pages: int, v_aliases_k: bool = False, num_ctas: int = 0,
-                     num_sms: int = 0) -> Plan:
+                     num_sms: int = 0, kv_dtype: int = 0) -> Plan:
     prob = Problem(max_bs=max_bs, max_draft=max_draft, num_q_heads=num_q_heads,
                    num_kv_heads=num_kv_heads, qk_dim=qk_dim, v_dim=v_dim, page_size=page_size,
                    dtype=dtype, v_aliases_k=int(bool(v_aliases_k)), num_ctas=num_ctas,
-                   num_sms=num_sms, max_kv_len=max_kv_len, num_pages=num_pages)
+                   num_sms=num_sms, kv_dtype=kv_dtype, max_kv_len=max_kv_len, num_pages=num_pages)
     plan = Plan()
     rc = load_library().verify_attn_plan(ctypes.byref(prob), ctypes.byref(plan))
     if rc != VA_OK:
@@ -181,6 +185,33 @@ def verify_attn_build_page_table(bs: int, page_size: int, num_pages: int, kv_ind
         _ptr(error_word), _stream_handle(stream))
     if rc != VA_OK:
         raise VerifyAttnError(rc, "verify_attn_build_page_table")
+
+
+def _event_handles(events):
+    if events is None:
+        return None
+    handles = []
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+            e.record()
+        handles.append(e.cuda_event)
+    return (ctypes.c_void_p * 4)(*handles)
+
+
+def verify_attn_paged_scaled(plan: Plan, bs: int, q, k_cache, v_cache, page_table, kv_indptr, seq_lens,
+                             num_draft, tree_mask, page_size: int, scale: float, window: int,
+                             k_scale: float, v_scale: float, out, lse, workspace, stream=None,
+                             events=None) -> None:
+    """Calls verify_attn_paged_scaled: per-tensor K/V dequantisation scales (an
+    FP8 plan's pools) and an optional tree mask; raises VerifyAttnError on a
+    nonzero status."""
+    rc = load_library().verify_attn_paged_scaled(
+        ctypes.byref(plan), int(bs), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+        _ptr(kv_indptr), _ptr(seq_lens), _ptr(num_draft), _ptr(tree_mask), int(page_size), float(scale),
+        int(window), float(k_scale), float(v_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        _stream_handle(stream), _event_handles(events))
+    if rc != VA_OK:
+        raise VerifyAttnError(rc, "verify_attn_paged_scaled")
 
 
 def verify_attn_paged_tree(plan: Plan, bs: int, q, k_cache, v_cache, page_table, kv_indptr, seq_lens,

@@ -24,16 +24,23 @@ cudaError_t launch_prefix_mma_64x64(const CUtensorMap&, const CUtensorMap&, cons
 cudaError_t launch_prefix_mma_128x128(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
 cudaError_t launch_prefix_mma_192x128(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
 cudaError_t launch_prefix_mma_256x256(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
+cudaError_t launch_prefix_mma8_128x128(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
+cudaError_t launch_prefix_mma8_256x256(const CUtensorMap&, const CUtensorMap&, const Args&, const Geo&, int, cudaStream_t);
 bool mla_available();
 
-static MmaLaunch mma_launcher(int qk, int v) {
+static MmaLaunch mma_launcher(int qk, int v, bool kv8) {
+    if (kv8) {
+        if (qk == 128 && v == 128) return launch_prefix_mma8_128x128;
+        if (qk == 256 && v == 256) return launch_prefix_mma8_256x256;
+        return nullptr;
+    }
     if (qk == 64 && v == 64) return launch_prefix_mma_64x64;
     if (qk == 128 && v == 128) return launch_prefix_mma_128x128;
     if (qk == 192 && v == 128) return launch_prefix_mma_192x128;
     if (qk == 256 && v == 256) return launch_prefix_mma_256x256;
     return nullptr;
 }
-bool prefix_mma_built(int qk, int v) { return mma_launcher(qk, v) != nullptr; }
+bool prefix_mma_built(int qk, int v, bool kv8) { return mma_launcher(qk, v, kv8) != nullptr; }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against the driver library); looked up once.
@@ -59,12 +66,15 @@ static bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, int c
                             int64_t slots, int hkv, int tb, int hg) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    // boxes of 128-byte rows: 64 columns of a 16-bit pool, 128 of an FP8 pool
+    const int esize = dtype == VA_FP8_E4M3 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)slots, (cuuint64_t)hkv};
-    const cuuint64_t strides[2] = {(cuuint64_t)hkv * row_elems * 2, (cuuint64_t)row_elems * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)tb, (cuuint32_t)hg};
+    const cuuint64_t strides[2] = {(cuuint64_t)hkv * row_elems * esize, (cuuint64_t)row_elems * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), (cuuint32_t)tb, (cuuint32_t)hg};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        dtype == VA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = dtype == VA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == VA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -109,6 +119,10 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         p.num_pages < 1 || p.num_ctas < 0 || p.num_sms < 0)
         return VA_INVALID_ARG;
     if (p.dtype != VA_FP32 && p.dtype != VA_BF16 && p.dtype != VA_FP16) return VA_INVALID_ARG;
+    if (p.kv_dtype != 0 && p.kv_dtype != VA_FP8_E4M3) return VA_INVALID_ARG;
+    const bool kv8 = p.kv_dtype == VA_FP8_E4M3;
+    if (kv8 && (p.dtype == VA_FP32 || p.v_aliases_k || p.qk_dim % 128 || p.v_dim % 128))
+        return VA_UNSUPPORTED;
     if (p.v_aliases_k && p.v_dim > p.qk_dim) return VA_INVALID_ARG;
     if ((int64_t)p.max_bs * p.num_kv_heads > 65535) return VA_UNSUPPORTED;   // combine grid.y
     if (!va::combine_supported(p.qk_dim, p.v_dim)) return VA_UNSUPPORTED;
@@ -128,7 +142,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.path = VA_PATH_F32;
         ctas_per_sm = smem <= 100 * 1024 ? 2 : 1;
         out.tile_tokens = va::kTile;
-    } else if (p.v_aliases_k && p.num_kv_heads == 1 && p.num_q_heads == 128 && p.qk_dim == 576 &&
+    } else if (!kv8 && p.v_aliases_k && p.num_kv_heads == 1 && p.num_q_heads == 128 && p.qk_dim == 576 &&
                p.v_dim == 512 && p.dtype == VA_BF16 && va::mla_available() &&
                va::mla_page_size_ok(p.page_size)) {
         // absorbed MLA: 64-token tiles, one 2-CTA cluster per 128-row block
@@ -142,16 +156,28 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         // hg * mt <= 8 consumer warps) over 16-token tiles fed by TMA boxes of
         // gcd(page_size, 16) tokens
         const int mt = (out.rows_cap + 15) / 16;
-        if (mt > 8 || !va::prefix_mma_built(p.qk_dim, p.v_dim)) return VA_UNSUPPORTED;
-        int hg = 1;
-        for (int d = 1; d <= p.num_kv_heads && d * mt <= 8; ++d)
-            if (p.num_kv_heads % d == 0) hg = d;
+        if (mt > 8 || !va::prefix_mma_built(p.qk_dim, p.v_dim, kv8)) return VA_UNSUPPORTED;
+        // the most kv-heads per CTA (a divisor of Hkv, hg * mt <= 8 warps) that
+        // still leaves room for a ring of at least three stages (two at worst)
         const int tb = va::gcd_int(p.page_size, 16);
-        const int box_stride = (tb * hg * 128 + 1023) / 1024 * 1024;
-        const int stage = (p.qk_dim / 64 + p.v_dim / 64) * (16 / tb) * box_stride;
-        int stages = (kSmemLimit - 2048) / stage;
-        if (stages > 8) stages = 8;
-        if (stages < 2) return VA_UNSUPPORTED;
+        const int slice = kv8 ? 128 : 64;   // columns per 128-byte row
+        int hg = 0, box_stride = 0, stage = 0, stages = 0;
+        for (int want = 3; want >= 2 && hg == 0; --want) {
+            for (int d = 8; d >= 1; --d) {
+                if (p.num_kv_heads % d != 0 || d * mt > 8) continue;
+                const int bstr = (tb * d * 128 + 1023) / 1024 * 1024;
+                const int stg = (p.qk_dim / slice + p.v_dim / slice) * (16 / tb) * bstr;
+                // FP8: each consumer warp's fp16 copy of its head's tile (16 tokens)
+                const int staging = kv8 ? d * mt * (p.qk_dim / 64 + p.v_dim / 64) * 2048 : 0;
+                const int n = (kSmemLimit - 2048 - staging) / stg;
+                if (n >= want) {
+                    hg = d; box_stride = bstr; stage = stg; stages = n > 8 ? 8 : n;
+                    break;
+                }
+            }
+        }
+        if (hg == 0) return VA_UNSUPPORTED;
+        (void)box_stride;
         out.path = VA_PATH_MMA;
         out.variant = mt;
         out.tile_tokens = 16;
@@ -208,8 +234,11 @@ namespace va {
 int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
         const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
-        void* workspace, void* stream, void* const* events, const int32_t* tree_mask) {
+        void* workspace, void* stream, void* const* events, const int32_t* tree_mask, float k_scale,
+        float v_scale) {
     if (!plan) return VA_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale < INFINITY))
+        return VA_INVALID_ARG;
     if (tree_mask && (window >= 0 || !is_aligned(tree_mask, 4))) return VA_INVALID_ARG;
     const va_problem& p = plan->problem;
     if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_MLA || plan->num_ctas < 1 ||
@@ -266,7 +295,9 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.mla = plan->path == VA_PATH_MLA;
     if (a.hg < 1 || p.num_kv_heads % a.hg != 0) return VA_INVALID_ARG;
     a.scale = scale;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale_log2 = scale * k_scale * 1.4426950408889634f;
+    a.v_scale = v_scale;
+    const bool kv8 = p.kv_dtype == VA_FP8_E4M3;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     auto rec = [&](int i) {
@@ -290,20 +321,23 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         g.ppt = plan->tile_tokens / g.tb;
         g.box_stride = (g.tb * g.hg * 128 + 1023) / 1024 * 1024;
         g.half_bytes = g.ppt * g.box_stride;
-        g.nhk = p.qk_dim / 64;
-        g.nhv = p.v_dim / 64;
+        g.slice_cols = kv8 ? 128 : 64;
+        g.nhk = p.qk_dim / g.slice_cols;
+        g.nhv = p.v_dim / g.slice_cols;
         g.stage_bytes = plan->stage_bytes;
         g.stages = plan->stages;
+        g.staging_bytes = kv8 ? (p.qk_dim / 64 + p.v_dim / 64) * 2048 : 0;
         g.tx_box = (uint32_t)(g.tb * g.hg * 128);
-        const va::MmaLaunch fn = va::mma_launcher(p.qk_dim, p.v_dim);
+        const va::MmaLaunch fn = va::mma_launcher(p.qk_dim, p.v_dim, kv8);
         const int64_t slots = p.num_pages * p.page_size;
         CUtensorMap kmap, vmap;
         if (!fn || g.nc < 1 || g.nc > 8 || g.ppt * g.tb != plan->tile_tokens ||
             g.stage_bytes != (g.nhk + g.nhv) * g.half_bytes)
             return VA_INVALID_ARG;
-        if (!va::encode_pool_map(&kmap, a.k_cache, p.dtype, p.qk_dim, p.qk_dim, slots,
+        const int pool_dtype = kv8 ? VA_FP8_E4M3 : p.dtype;
+        if (!va::encode_pool_map(&kmap, a.k_cache, pool_dtype, p.qk_dim, p.qk_dim, slots,
                                  p.num_kv_heads, g.tb, g.hg) ||
-            !va::encode_pool_map(&vmap, a.v_cache, p.dtype, p.v_dim, (int)a.v_row_stride, slots,
+            !va::encode_pool_map(&vmap, a.v_cache, pool_dtype, p.v_dim, (int)a.v_row_stride, slots,
                                  p.num_kv_heads, g.tb, g.hg))
             return cuda_failure("tensor-map encoding", cudaErrorInvalidValue);
         e = fn(kmap, vmap, a, g, p.dtype, s);
@@ -336,7 +370,17 @@ extern "C" int verify_attn_paged_tree(const va_plan* plan, int bs, const void* q
                                       void* const events[4]) {
     if (!tree_mask) return VA_INVALID_ARG;
     return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft, page_size,
-                   scale, -1, out, lse, workspace, stream, events, tree_mask);
+                   scale, -1, out, lse, workspace, stream, events, tree_mask, 1.f, 1.f);
+}
+
+extern "C" int verify_attn_paged_scaled(const va_plan* plan, int bs, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* page_table,
+                                        const int32_t* kv_indptr, const int32_t* seq_lens,
+                                        const int32_t* num_draft, const int32_t* tree_mask, int page_size,
+                                        float scale, int window, float k_scale, float v_scale, void* out,
+                                        float* lse, void* workspace, void* stream, void* const events[4]) {
+    return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft, page_size,
+                   scale, window, out, lse, workspace, stream, events, tree_mask, k_scale, v_scale);
 }
 
 extern "C" int verify_attn_paged_profiled(const va_plan* plan, int bs, const void* q,

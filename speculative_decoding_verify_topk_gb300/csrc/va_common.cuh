@@ -78,8 +78,9 @@ struct Args {
     int hg;                  // kv-heads a prefix CTA handles together (1 on the fp32 path)
     int mla;                 // 1: absorbed-MLA layout (row blocks of 128 heads per draft,
                              //    2-CTA clusters, partial slots of 128 rows)
-    float scale_log2;        // scale * log2(e)
+    float scale_log2;        // scale * k_scale * log2(e)
     float scale;
+    float v_scale;           // per-tensor V dequantisation scale (1 unless a quantised cache)
 };
 
 // One verify call on a caller-provided workspace (validation + the three
@@ -87,7 +88,8 @@ struct Args {
 int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const void* v_cache,
         const int32_t* page_table, const int32_t* kv_indptr, const int32_t* seq_lens,
         const int32_t* num_draft, int page_size, float scale, int window, void* out, float* lse,
-        void* workspace, void* stream, void* const* events, const int32_t* tree_mask = nullptr);
+        void* workspace, void* stream, void* const* events, const int32_t* tree_mask = nullptr,
+        float k_scale = 1.f, float v_scale = 1.f);
 
 // Launches `kern` with programmatic stream serialization: it may begin while
 // the preceding kernel on the stream finishes, and must call pdl_wait()
@@ -114,9 +116,11 @@ struct Geo {
     int hg, mt, nc;        // heads per CTA, m16 tiles per head, consumer warps
     int tb, ppt;           // tokens per TMA box, boxes (page chunks) per tile
     int box_stride;        // bytes between boxes (box bytes rounded up to 1 KB)
-    int half_bytes;        // one 64-column slice of a tile: ppt * box_stride
-    int nhk, nhv;          // 64-column slices of K and of V rows
+    int half_bytes;        // one column slice (128-byte rows) of a tile: ppt * box_stride
+    int nhk, nhv;          // column slices of K and of V rows
+    int slice_cols;        // columns per slice: 64 (16-bit pools), 128 (FP8 pools)
     int stage_bytes, stages;
+    int staging_bytes;     // FP8 pools: per consumer warp, its head's tile converted to fp16
     uint32_t tx_box;       // bytes one box delivers
 };
 
@@ -129,7 +133,7 @@ size_t prefix_f32_smem_bytes(int qk_dim, int v_dim, int rows_cap);
 bool combine_supported(int qk_dim, int v_dim);
 int mla_stages();
 bool mla_page_size_ok(int page_size);
-bool prefix_mma_built(int qk_dim, int v_dim);
+bool prefix_mma_built(int qk_dim, int v_dim, bool kv8);
 
 // ---------------------------------------------------------------------------
 // Device helpers

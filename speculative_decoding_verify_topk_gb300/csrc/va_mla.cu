@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (seg_end) {
                     wait_or_abort(b_pvdone, k & 1, 11);
                     tc_fence_after();
-                    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+                    const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;   // times the V dequant scale
                     const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
                     float* po = a.part_o + (slot * kRows + row) * kV + rank * (kV / 2);
                     uint32_t r[32];

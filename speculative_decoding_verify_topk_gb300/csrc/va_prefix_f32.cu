@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
             const int64_t slot = partial_slot(a, cur.g, cur.b, cta);
             for (int r = warp; r < rows_b; r += kWarps) {
                 const float l = ls[r];
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? a.v_scale / l : 0.f;   // times the V dequantisation scale
                 float* po = a.part_o + ((int64_t)slot * a.rows_cap + r) * dv;
                 for (int d = lane; d < dv; d += 32) po[d] = os[r * dv + d] * inv;
                 if (lane == 0)

@@ -33,6 +33,15 @@
 //   * V rows of tokens at or past P_b + D_b may hold another sequence's data
 //     or garbage; in the tiles that reach that far each consumer zeroes its
 //     head's V rows there before P V (0 * NaN would poison the sum).
+//   * FP8 E4M3 pools (KV8): boxes carry 128 one-byte columns per 128-byte
+//     row, halving the HBM bytes. Each consumer warp converts its head's tile
+//     (every E4M3 value is exact in fp16) into a private fp16 staging area
+//     with the same swizzled layout, releases the stage at once, and runs the
+//     fp16 tensor-core path on it with the query converted to fp16 at a
+//     segment start. k_scale is folded into the softmax scale and v_scale into
+//     the partial output ("Split-KV flash-decode attention ...",
+//     Modifications: the prefix stage applies the fp8 k_scale / v_scale
+//     dequant multipliers).
 // Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT
 // and the CTA winds down (no further waits) instead of hanging.
 #pragma once
@@ -40,6 +49,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "va_common.cuh"
 
@@ -94,6 +105,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& d0, uint32_t&
                  : "r"(addr));
 }
 
+// Two FP8 E4M3 values (low byte first) -> two fp16 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(d) : "h"(x));
+    return d;
+}
+
 // 3-d tiled TMA load: box at coordinates {col, token slot, head} -> shared.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
@@ -104,19 +122,35 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// A pair of query elements as the tensor-core operand: unchanged, or (over an
+// FP8 cache, where the MMA runs in fp16) converted from bf16 / fp16 to fp16.
+template <typename T, bool KV8>
+__device__ __forceinline__ uint32_t to_mma_pair(uint32_t x) {
+    if constexpr (!KV8 || std::is_same<T, __half>::value) {
+        return x;
+    } else {
+        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&x);
+        __half2 h = __float22half2_rn(__bfloat1622float2(b));
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
 constexpr int kTT = 16;            // tokens per tile
 constexpr int kMaxConsumers = 8;   // consumer warps per CTA (HG * MT)
 constexpr int kThreads = (kMaxConsumers + 1) * 32;
 
-template <typename T, int DQK, int DV>
+template <typename T, int DQK, int DV, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, Args a, Geo geo) {
+    // tensor-core operand type: the query's, or fp16 over an FP8 cache
+    using MT = typename std::conditional<KV8, __half, T>::type;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB alignment for the 128-byte swizzle atoms
     unsigned char* const ring =
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char* const bars = ring + geo.stages * geo.stage_bytes;
+    unsigned char* const staging = ring + geo.stages * geo.stage_bytes;   // KV8: nc areas
+    unsigned char* const bars = staging + geo.nc * geo.staging_bytes;
     const uint32_t bar_full = smem_u32(bars);                 // [stages], count 1 (+ tx)
     const uint32_t bar_empty = bar_full + 8 * geo.stages;     // [stages], count nc
     __shared__ int abort_flag;
@@ -212,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = page * a.page_size + off;
                 const uint32_t dst = sbase + part * geo.half_bytes + c * geo.box_stride;
                 if (part < geo.nhk)
-                    tma_load_3d(dst, &kmap, part * 64, slot, cur.g * geo.hg, full);
+                    tma_load_3d(dst, &kmap, part * geo.slice_cols, slot, cur.g * geo.hg, full);
                 else
-                    tma_load_3d(dst, &vmap, (part - geo.nhk) * 64, slot, cur.g * geo.hg, full);
+                    tma_load_3d(dst, &vmap, (part - geo.nhk) * geo.slice_cols, slot, cur.g * geo.hg, full);
             }
             if (k + 1 < n_tiles) {
                 n_page = p_page; n_off = p_off; n_valid = p_valid;
@@ -278,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int kk = 0; kk < DQK / 16; ++kk) {
-                        qf[kk][h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + c2)) : 0u;
-                        qf[kk][2 + h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 8 + c2)) : 0u;
+                        qf[kk][h] = live ? to_mma_pair<T, KV8>(__ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + c2))) : 0u;
+                        qf[kk][2 + h] = live ? to_mma_pair<T, KV8>(__ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 8 + c2))) : 0u;
                     }
                 }
 #pragma unroll
@@ -299,14 +333,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
             unsigned char* const stage = ring + st * geo.stage_bytes;
-            const uint32_t kbase = smem_u32(stage);
-            const uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
+            uint32_t kbase = smem_u32(stage);
+            uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
+            uint32_t half_stride = geo.half_bytes;
             const int tile_j0 = si.a0 + cur.t * kTT;
 
             // V rows of tokens past the sequence's end: zero them (this head)
             const int seq_end = si.prefix + si.draft;
             const bool tail = tile_j0 + kTT > seq_end;
-            if (tail) {
+            if constexpr (KV8) {
+                // this head's K and V rows, FP8 -> fp16, into the warp's staging
+                // area: slices of 64 columns, [slice][16 tokens][128 B], the same
+                // 16-byte-chunk swizzle. Rows no query can see -- past the
+                // sequence's end, or before the window's first key -- become
+                // zeros: their stage bytes may be another tile's leftovers
+                // (boxes wholly outside the visible keys are not refilled)
+                unsigned char* const stg = staging + warp * geo.staging_bytes;
+                __syncwarp();   // the previous tile's ldmatrix reads are done
+                constexpr int kItems = kTT * (DQK + DV) / 16;   // 16-byte FP8 chunks
+#pragma unroll
+                for (int it = lane; it < kItems; it += 32) {
+                    const int t = it & (kTT - 1), c16 = it / kTT;   // token, 16-column chunk
+                    const bool is_k = c16 < DQK / 16;
+                    const int cc = is_k ? c16 : c16 - DQK / 16;     // chunk within K or V
+                    const int part = cc >> 3, c8 = cc & 7;          // 128-column slice, chunk in it
+                    const uint32_t src = smem_u32(stage) + (is_k ? 0 : geo.nhk * geo.half_bytes) +
+                                         part * geo.half_bytes + rowaddr(t, c8);
+                    uint4 x = make_uint4(0, 0, 0, 0);
+                    if (tile_j0 + t < seq_end && tile_j0 + t >= si.lo)
+                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                                     : "r"(src));
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        h[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
+                        h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
+                    }
+                    const int col = cc * 16;                        // first column of the chunk
+                    const int sl = col >> 6, ch0 = (col & 63) >> 3; // fp16 slice, 16-byte chunk
+                    unsigned char* const drow = stg + (is_k ? 0 : (DQK / 64) * 2048) + sl * 2048 + t * 128;
+                    *reinterpret_cast<uint4*>(drow + ((ch0 ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4*>(drow + (((ch0 + 1) ^ (t & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);   // the stage is no longer read
+                kbase = smem_u32(stg);
+                vbase = kbase + (DQK / 64) * 2048;
+                half_stride = 2048;
+            } else if (tail) {
                 for (int idx = lane; idx < kTT * geo.nhv * 8; idx += 32) {
                     const int t = idx / (geo.nhv * 8), rem = idx - t * geo.nhv * 8;
                     const int h = rem >> 3, ch = rem & 7;
@@ -317,6 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
 
+            // byte offset of 16-byte chunk ch of token t inside one 64-column slice
+            auto opaddr = [&](int t, int ch) -> uint32_t {
+                if constexpr (KV8) return (uint32_t)(t * 128 + ((ch ^ (t & 7)) << 4));
+                else return rowaddr(t, ch);
+            };
             // ---- S = Q K^T over the tile's 16 tokens (two n8 tiles)
             float s[2][4];
 #pragma unroll
@@ -326,9 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tok = (mi >> 1) * 8 + r8;
                 const int ch = (kk & 3) * 2 + (mi & 1);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + (kk >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
-                Mma<T>::run(s[0], qf[kk], b0, b1);
-                Mma<T>::run(s[1], qf[kk], b2, b3);
+                ldsm_x4(kbase + (kk >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
+                Mma<MT>::run(s[0], qf[kk], b0, b1);
+                Mma<MT>::run(s[1], qf[kk], b2, b3);
             }
 
             // ---- scale, mask, online softmax (rows lane/4 and lane/4 + 8 of the m-tile)
@@ -384,25 +465,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- O += P V
             {
                 uint32_t pa[4];
-                pa[0] = Mma<T>::pack(s[0][0], s[0][1]);
-                pa[1] = Mma<T>::pack(s[0][2], s[0][3]);
-                pa[2] = Mma<T>::pack(s[1][0], s[1][1]);
-                pa[3] = Mma<T>::pack(s[1][2], s[1][3]);
+                pa[0] = Mma<MT>::pack(s[0][0], s[0][1]);
+                pa[1] = Mma<MT>::pack(s[0][2], s[0][3]);
+                pa[2] = Mma<MT>::pack(s[1][0], s[1][1]);
+                pa[3] = Mma<MT>::pack(s[1][2], s[1][3]);
                 const int tok = (mi & 1) * 8 + r8;
 #pragma unroll
                 for (int nd = 0; nd < DV / 16; ++nd) {
                     const int ch = (nd & 3) * 2 + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vbase + (nd >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
-                    Mma<T>::run(o[2 * nd], pa, b0, b1);
-                    Mma<T>::run(o[2 * nd + 1], pa, b2, b3);
+                    ldsm_x4_t(vbase + (nd >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
+                    Mma<MT>::run(o[2 * nd], pa, b0, b1);
+                    Mma<MT>::run(o[2 * nd + 1], pa, b2, b3);
                 }
             }
             // release the stage; zeroed rows (generic writes) are ordered before
-            // the next fill's bulk-tensor writes
-            if (tail) fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            // the next fill's bulk-tensor writes (KV8 released it after converting)
+            if constexpr (!KV8) {
+                if (tail) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
 
             if (seg_end) {
 #pragma unroll
@@ -411,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
                 }
                 const int r0 = lane >> 2, c0 = 2 * (lane & 3);
-                const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
-                const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+                // normalised partial output, times the V dequantisation scale
+                const float inv0 = l_run[0] > 0.f ? a.v_scale / l_run[0] : 0.f;
+                const float inv1 = l_run[1] > 0.f ? a.v_scale / l_run[1] : 0.f;
                 const int64_t slot = partial_slot(a, g, cur.b, cta);
                 const int rr0 = wm * 16 + r0, rr1 = rr0 + 8;
                 float* po = a.part_o + (int64_t)slot * a.rows_cap * DV;
@@ -437,11 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 }
 
-template <typename T, int DQK, int DV>
+template <typename T, int DQK, int DV, bool KV8 = false>
 cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, const Geo& g,
                    cudaStream_t s) {
-    auto kern = prefix_mma_kernel<T, DQK, DV>;
-    const int smem = 1024 + g.stages * g.stage_bytes + 16 * g.stages;
+    auto kern = prefix_mma_kernel<T, DQK, DV, KV8>;
+    const int smem = 1024 + g.stages * g.stage_bytes + g.nc * g.staging_bytes + 16 * g.stages;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + 1) * 32), smem, s, kmap, vmap, a, g);

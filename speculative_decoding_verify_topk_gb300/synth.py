@@ -95,6 +95,12 @@ WORKLOADS = {
     "draft_extend": Workload("draft_extend", torch.bfloat16, 64, 32, 8, 128, 128, 16,
                              ("uniform", 1024, 8192), ("choice", [1, 2, 3, 4, 5]), 5,
                              1.0 / math.sqrt(128)),
+    # the Llama-3.1-8B-shaped batch over an FP8 E4M3 KV cache with per-tensor
+    # scales (K / k_scale and V / v_scale stored)
+    "llama8b_fp8": Workload("llama8b_fp8", torch.bfloat16, 16, 32, 8, 128, 128, 4,
+                            ("uniform", 1024, 8192), ("fixed", 4), 1, 1.0 / math.sqrt(128),
+                            pool_tokens=1 << 21, kv_dtype=torch.float8_e4m3fn, k_scale=0.5,
+                            v_scale=0.5),
     # tree verify at topk > 1: the Llama-3.1-8B-shaped batch with 8 draft tokens
     # per sequence forming a random tree (each row sees its ancestors)
     "llama8b_tree": Workload("llama8b_tree", torch.bfloat16, 16, 32, 8, 128, 128, 4,

@@ -92,6 +92,28 @@ def test_plan_selects_paths(lib):
     assert _plan(num_ctas=7).num_ctas == 7
 
 
+def test_plan_fp8_pools(lib):
+    """FP8 E4M3 pools: 128 one-byte columns per 128-byte box row (half the stage
+    bytes of bf16), plus an fp16 staging area per consumer warp."""
+    p = _plan(kv_dtype=va.VA_FP8_E4M3)
+    assert p.path == va.VA_PATH_MMA and p.heads_per_cta == 8 and p.box_tokens == 4
+    assert p.stage_bytes == (1 + 1) * 4 * (4 * 8 * 128)      # one 128-column slice of K and of V
+    assert p.stage_bytes == _plan().stage_bytes // 2
+    staging = 8 * (2 + 2) * 2048                              # 8 warps x (K + V) 64-column slices
+    assert 2 <= p.stages <= 8 and p.stages * p.stage_bytes + staging <= 227 * 1024 - 2048
+    assert _plan(kv_dtype=va.VA_FP8_E4M3, dtype=va.VA_FP16, qk_dim=256, v_dim=256).path == va.VA_PATH_MMA
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=va.VA_FP32), dict(qk_dim=64, v_dim=64),
+                                dict(qk_dim=192, v_dim=128), dict(v_aliases_k=True, num_kv_heads=1,
+                                                                  num_q_heads=128, qk_dim=576,
+                                                                  v_dim=512, page_size=64)])
+def test_plan_fp8_unsupported_shapes(lib, kw):
+    with pytest.raises(va.VerifyAttnError) as e:
+        _plan(kv_dtype=va.VA_FP8_E4M3, **kw)
+    assert e.value.status == binding.VA_UNSUPPORTED
+
+
 def test_workspace_depends_on_max_bs_only(lib):
     a, b = _plan(max_kv_len=1 << 20), _plan(max_kv_len=4096)
     assert a.workspace_bytes == b.workspace_bytes
@@ -101,7 +123,7 @@ def test_workspace_depends_on_max_bs_only(lib):
 @pytest.mark.parametrize("kw", [dict(num_q_heads=30, num_kv_heads=8), dict(max_draft=0),
                                 dict(max_bs=0), dict(page_size=0), dict(dtype=7),
                                 dict(v_aliases_k=True, qk_dim=64, v_dim=128),
-                                dict(max_draft=33), dict(num_pages=0)])
+                                dict(max_draft=33), dict(num_pages=0), dict(kv_dtype=2)])
 def test_plan_rejects_invalid(lib, kw):
     with pytest.raises(va.VerifyAttnError) as e:
         _plan(**kw)
