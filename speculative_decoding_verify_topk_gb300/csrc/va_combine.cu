@@ -12,8 +12,11 @@
 //
 // One warp per query row (grid: row blocks of 8 x (bs * Hkv)). Lane l owns the
 // output columns [l * VPL, (l + 1) * VPL), so every partial row is read as one
-// coalesced run; the segments' lse values are read lane-parallel first, then
-// the partial rows are streamed four at a time.
+// coalesced run. The segments' lse values (lane-parallel) and the first batch
+// of partial rows are loaded in one round -- no load waits on a weight -- and
+// the rest in batches. The sequence table and tile count come from the work
+// list, which finished before the prefix kernel started its work, so they are
+// read before the wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -55,13 +58,16 @@ __device__ __forceinline__ void load_f32(const float* p, float (&v)[VPL]) {
 // columns per lane (compile-time: the loops below carry no predicates).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
-    pdl_wait();   // partials of the prefix kernel (and the work list) are ready
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int bg = blockIdx.y;
     const int b = bg / a.hkv, g = bg - b * a.hkv;
+    // The work list finished before the prefix kernel began its work, so its
+    // sequence table is complete here; only the partials need the wait.
     const SeqInfo si = a.seq[b];
+    const int total_tiles = a.header[kHdrTotalTiles];
     const int rows_b = a.group * si.draft;
     const int r = blockIdx.x * kWarps + warp;
+    pdl_wait();   // partials of the prefix kernel are ready
     if (r >= rows_b) return;
     const int i = r / a.group, h = g * a.group + (r - i * a.group);
     const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + h;
@@ -77,7 +83,6 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     // partition. GQA: the stream is over (head group, sequence, tile) and the
     // workers are CTAs; MLA: over (row block = draft, sequence, tile) and the
     // workers are 2-CTA clusters, whose slots hold 128 rows.
-    const int total_tiles = a.header[kHdrTotalTiles];
     int64_t work, x0, slot0, slot_rows, prow;
     int workers;
     if (a.mla) {
@@ -103,16 +108,26 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
                (all_busy || cta_start(c + 1, work, workers) != cta_start(c, work, workers));
     };
 
-    // ---- M: the largest partial lse
+    // ---- one round of independent loads: the segments' lse values (lane c
+    // holds segment c_first + c) and the first batch of partial rows; only
+    // then the max, the weights and the sums
+    constexpr int kBatch = VPL <= 8 ? 8 : 4;   // partial rows in flight per round
+    auto row_ptr = [&](int c) {
+        return a.part_o + ((slot0 + c) * slot_rows + prow) * (VPL * 32) + lane * VPL;
+    };
     const float lse_first = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * slot_rows + prow]
                                                  : -INFINITY;
+    float v[kBatch][VPL];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        if (live(c_first + u)) load_f32<VPL>(row_ptr(c_first + u), v[u]);
     float mx = lse_first;
-    for (int c = c_first + 32 + lane; c <= c_last; c += 32)
+    for (int c = c_first + 32 + lane; c <= c_last; c += 32)   // more than 32 segments: rare
         if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * slot_rows + prow]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
-    // ---- weighted sum of the partial rows
+    // ---- weighted sum of the partial rows (a segment with lse = -inf weighs 0)
     float acc[VPL];
 #pragma unroll
     for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
@@ -126,21 +141,20 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
         }
         z += w;
         const int n = c_last - cb + 1 < 32 ? c_last - cb + 1 : 32;
-        for (int j = 0; j < n; j += 4) {   // four independent row loads in flight
-            float v[4][VPL], wj[4];
+        for (int j = 0; j < n; j += kBatch) {
+            if (cb != c_first || j != 0) {   // the first batch is already in registers
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
-                if (j + u < n && wj[u] != 0.f)
-                    load_f32<VPL>(a.part_o + ((slot0 + cb + j + u) * slot_rows + prow) * (VPL * 32) +
-                                      lane * VPL, v[u]);
+                for (int u = 0; u < kBatch; ++u)
+                    if (j + u < n && live(cb + j + u)) load_f32<VPL>(row_ptr(cb + j + u), v[u]);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (j + u < n && wj[u] != 0.f) {
+            for (int u = 0; u < kBatch; ++u) {
+                const float wj = __shfl_sync(0xffffffffu, w, (j + u) & 31);
+                if (j + u < n && wj != 0.f) {
 #pragma unroll
-                    for (int e = 0; e < VPL; ++e) acc[e] = fmaf(wj[u], v[u][e], acc[e]);
+                    for (int e = 0; e < VPL; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
                 }
+            }
         }
     }
 #pragma unroll

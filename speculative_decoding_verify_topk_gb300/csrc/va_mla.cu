@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_2d_pair(smem_u32(stg + c * kTok * 128 + q * geo.tb * 128), &kmap, c * kChunk,
                                         slot[q], b_kfull + 8 * st);
                     }
+                    // the combine may launch while this CTA drains its ring
+                    if (k + 1 == n_tiles) pdl_launch_dependents();
                     if (k + 1 < n_tiles) cur.advance(a);
                 }
             }

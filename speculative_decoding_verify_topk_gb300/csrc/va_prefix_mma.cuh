@@ -105,6 +105,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& d0, uint32_t&
                  : "r"(addr));
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Two FP8 E4M3 values (low byte first) -> two fp16 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     uint32_t d;
@@ -250,6 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     tma_load_3d(dst, &vmap, (part - geo.nhk) * geo.slice_cols, slot, cur.g * geo.hg, full);
             }
+            // the combine may launch once every CTA has issued its last tile's
+            // loads: its CTAs then start while the ring drains (releasing it at
+            // the start parked them on the SMs for the whole run, which
+            // measured slower)
+            if (k + 1 == n_tiles) pdl_launch_dependents();
             if (k + 1 < n_tiles) {
                 n_page = p_page; n_off = p_off; n_valid = p_valid;
                 if (k + 2 < n_tiles) {
@@ -398,19 +409,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (KV8) return (uint32_t)(t * 128 + ((ch ^ (t & 7)) << 4));
                 else return rowaddr(t, ch);
             };
-            // ---- S = Q K^T over the tile's 16 tokens (two n8 tiles)
-            float s[2][4];
+            // ---- S = Q K^T over the tile's 16 tokens (two n8 tiles); even and odd
+            //      k-steps accumulate separately, halving the dependent MMA chain
+            float s[2][4], s2[2][4];
 #pragma unroll
-            for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[n][e] = s2[n][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
                 const int tok = (mi >> 1) * 8 + r8;
                 const int ch = (kk & 3) * 2 + (mi & 1);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + (kk >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
-                Mma<MT>::run(s[0], qf[kk], b0, b1);
-                Mma<MT>::run(s[1], qf[kk], b2, b3);
+                float (&acc)[2][4] = (kk & 1) ? s2 : s;
+                Mma<MT>::run(acc[0], qf[kk], b0, b1);
+                Mma<MT>::run(acc[1], qf[kk], b2, b3);
             }
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[n][e] += s2[n][e];
 
             // ---- scale, mask, online softmax (rows lane/4 and lane/4 + 8 of the m-tile)
             const bool need_mask = tile_j0 + kTT > si.prefix ||
@@ -432,34 +451,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx[e >> 1] = fmaxf(mx[e >> 1], v);
                 }
             }
+            // lazy rescaling: the reference max m_run moves only when a row's max
+            // exceeds it by more than 2^8, so most tiles skip the O rescale (P
+            // stays below 2^8: no loss in bf16 / fp16, fp32 sums)
             float alpha[2], m_use[2];
+            bool grow_any = false;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                const float m_new = fmaxf(m_run[h], mx[h]);
-                m_use[h] = m_new == -INFINITY ? 0.f : m_new;
-                alpha[h] = exp2f(m_run[h] - m_use[h]);
-                m_run[h] = m_new;
+                alpha[h] = 1.f;
+                if (mx[h] > m_run[h] + 8.f) {
+                    alpha[h] = ex2_approx(m_run[h] - mx[h]);   // 0 when m_run is -inf
+                    m_run[h] = mx[h];
+                    grow_any = true;
+                }
+                m_use[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];
             }
             float psum[2] = {0.f, 0.f};
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p = exp2f(s[n][e] - m_use[e >> 1]);
+                    const float p = ex2_approx(s[n][e] - m_use[e >> 1]);
                     s[n][e] = p;
                     psum[e >> 1] += p;
                 }
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + psum[h];
+            if (grow_any) {
 #pragma unroll
-            for (int n = 0; n < DV / 8; ++n) {
-                o[n][0] *= alpha[0];
-                o[n][1] *= alpha[0];
-                o[n][2] *= alpha[1];
-                o[n][3] *= alpha[1];
+                for (int n = 0; n < DV / 8; ++n) {
+                    o[n][0] *= alpha[0];
+                    o[n][1] *= alpha[0];
+                    o[n][2] *= alpha[1];
+                    o[n][3] *= alpha[1];
+                }
             }
 
             // ---- O += P V
@@ -518,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k + 1 < n_tiles) cur.advance(a);
         }
     }
-    pdl_launch_dependents();
+    pdl_launch_dependents();   // (again, harmless) for warps that issued no loads
 }
 
 template <typename T, int DQK, int DV, bool KV8 = false>
