@@ -50,6 +50,7 @@ KERNEL_SOURCES = {  # files whose change invalidates a stored ncu traffic figure
     "prefix_mma": ["va_prefix_mma.cuh", "va_common.cuh"],
     "prefix_f32": ["va_prefix_f32.cu", "va_common.cuh"],
     "prefix_mla": ["va_mla.cu", "va_common.cuh"],
+    "prefix_tc": ["va_prefix_tc.cu", "va_tc.cuh", "va_common.cuh"],
 }
 
 
@@ -493,7 +494,7 @@ def ours_arm(args):
         builder["frac_of_measured_hbm"] = builder["gbs"] / hbm_peak
     prefix_avg_ms = statistics.fmean(prefix_ms)
     kernel = {va.VA_PATH_MMA: "prefix_mma", va.VA_PATH_F32: "prefix_f32",
-              va.VA_PATH_MLA: "prefix_mla"}[attn.plan.path]
+              va.VA_PATH_MLA: "prefix_mla", va.VA_PATH_TC: "prefix_tc"}[attn.plan.path]
     traffic = stored_traffic(kernel, wl.name)
     achieved = acct["prefix_bytes"] / (prefix_avg_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

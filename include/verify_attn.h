@@ -55,8 +55,10 @@ enum va_dtype { VA_FP32 = 0, VA_BF16 = 1, VA_FP16 = 2, VA_FP8_E4M3 = 3 };
 /* Which prefix kernel a plan selects. */
 enum va_path {
     VA_PATH_F32 = 1,     /* fp32 inputs: CUDA-core kernel */
-    VA_PATH_MMA = 2,     /* bf16 / fp16 GQA: warp-level tensor-core tiles */
-    VA_PATH_MLA = 3      /* absorbed MLA (one latent kv-head, V aliases K): tcgen05 + TMEM */
+    VA_PATH_MMA = 2,     /* bf16 / fp16 GQA: warp-level tensor-core tiles (any page size, FP8 pools) */
+    VA_PATH_MLA = 3,     /* absorbed MLA (one latent kv-head, V aliases K): tcgen05 + TMEM */
+    VA_PATH_TC = 4       /* bf16 / fp16 GQA on tcgen05 + TMEM: page sizes that are multiples of 8,
+                            up to 128 query rows per kv-head (Hq / Hkv * max_draft) */
 };
 
 /* Bits of the device error word that verify_attn_check reports. A sequence

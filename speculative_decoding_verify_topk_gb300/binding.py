@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libverify_attn.so")
 
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_WORKSPACE_TOO_SMALL, VA_CUDA_ERROR, VA_DEVICE_RANGE_ERROR = range(6)
 VA_FP32, VA_BF16, VA_FP16, VA_FP8_E4M3 = 0, 1, 2, 3
-VA_PATH_F32, VA_PATH_MMA, VA_PATH_MLA = 1, 2, 3
+VA_PATH_F32, VA_PATH_MMA, VA_PATH_MLA, VA_PATH_TC = 1, 2, 3, 4
 VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR_TIMEOUT = 1, 2, 4, 8, 16
 
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",

@@ -151,6 +151,20 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.heads_per_cta = 1;
         out.stages = va::mla_stages();
         ctas_per_sm = 1;
+    } else if (!kv8 && out.rows_cap > 32 && out.rows_cap <= 128 && va::prefix_tc_built(p.qk_dim, p.v_dim) &&
+               va::prefix_tc_page_size_ok(p.page_size) && va::prefix_tc_stages(p.qk_dim, p.v_dim) >= 2) {
+        // bf16 / fp16 GQA on tcgen05: one kv-head per CTA at a time, 64-token
+        // tiles. Chosen above 32 query rows per kv-head, where the warp-level
+        // kernel needs three or more 16-row MMA tiles per head and turns
+        // latency-bound; with fewer rows it streams several kv-heads per tile
+        // and keeps the lead.
+        out.path = VA_PATH_TC;
+        out.tile_tokens = 64;
+        out.heads_per_cta = 1;
+        out.box_tokens = va::gcd_int(p.page_size, 64);
+        out.stages = va::prefix_tc_stages(p.qk_dim, p.v_dim);
+        out.stage_bytes = (p.qk_dim / 64 + p.v_dim / 64) * 64 * 128;
+        ctas_per_sm = 1;
     } else {
         // bf16 / fp16: a CTA takes hg kv-heads (the largest divisor of Hkv with
         // hg * mt <= 8 consumer warps) over 16-token tiles fed by TMA boxes of
@@ -241,7 +255,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         return VA_INVALID_ARG;
     if (tree_mask && (window >= 0 || !is_aligned(tree_mask, 4))) return VA_INVALID_ARG;
     const va_problem& p = plan->problem;
-    if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_MLA || plan->num_ctas < 1 ||
+    if (plan->path < VA_PATH_F32 || plan->path > VA_PATH_TC || plan->num_ctas < 1 ||
         plan->rows_cap < 1 || plan->workspace_bytes == 0 || plan->tile_tokens < 1)
         return VA_INVALID_ARG;
     if (bs < 0) return VA_INVALID_ARG;
@@ -312,6 +326,17 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     switch (plan->path) {
     case VA_PATH_F32: e = va::launch_prefix_f32(a, s); break;
     case VA_PATH_MLA: e = va::launch_prefix_mla(a, s); break;
+    case VA_PATH_TC: {
+        const int64_t slots = p.num_pages * p.page_size;
+        CUtensorMap kmap, vmap;
+        if (!va::encode_pool_map(&kmap, a.k_cache, p.dtype, p.qk_dim, p.qk_dim, slots, p.num_kv_heads,
+                                 plan->box_tokens, 1) ||
+            !va::encode_pool_map(&vmap, a.v_cache, p.dtype, p.v_dim, (int)a.v_row_stride, slots,
+                                 p.num_kv_heads, plan->box_tokens, 1))
+            return cuda_failure("tensor-map encoding", cudaErrorInvalidValue);
+        e = va::launch_prefix_tc(kmap, vmap, a, plan->stages, p.dtype, s);
+        break;
+    }
     default: {
         va::Geo g;
         g.hg = plan->heads_per_cta;

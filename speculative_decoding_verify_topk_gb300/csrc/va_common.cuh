@@ -26,6 +26,8 @@
 //     same partition formula.
 #pragma once
 
+#include <cuda.h>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -134,6 +136,11 @@ bool combine_supported(int qk_dim, int v_dim);
 int mla_stages();
 bool mla_page_size_ok(int page_size);
 bool prefix_mma_built(int qk_dim, int v_dim, bool kv8);
+bool prefix_tc_built(int qk_dim, int v_dim);
+int prefix_tc_stages(int qk_dim, int v_dim);
+bool prefix_tc_page_size_ok(int page_size);
+cudaError_t launch_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, int stages,
+                             int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -259,6 +266,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
+        // a rolled loop: the spin is on every waiter's instruction stream
+#pragma unroll 1
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > kWaitNs) return false;

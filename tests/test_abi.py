@@ -83,12 +83,33 @@ def test_plan_selects_paths(lib):
     assert p.workspace_bytes % 256 == 0 and p.workspace_bytes >= (
         p.off_part_o + 4 * p.num_slots * p.rows_cap * 128)
     assert _plan(dtype=va.VA_FP32, qk_dim=64, v_dim=64, num_q_heads=4, num_kv_heads=2).path == va.VA_PATH_F32
+    # more than 32 query rows per kv-head and page sizes that are multiples of 8
+    # go to the tcgen05 kernel: one kv-head per CTA, 64-token tiles, boxes of
+    # gcd(page_size, 64) tokens
     mixed = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128,
                   page_size=16)
-    assert mixed.path == va.VA_PATH_MMA and mixed.variant == 3  # 40 rows -> 3 m16 tiles
-    assert mixed.heads_per_cta == 2 and mixed.box_tokens == 16  # 2 heads x 3 tiles = 6 warps
-    assert _plan(page_size=1).box_tokens == 1 and _plan(page_size=64).box_tokens == 16
-    assert _plan(page_size=6).box_tokens == 2
+    assert mixed.path == va.VA_PATH_TC and mixed.rows_cap == 40 and mixed.tile_tokens == 64
+    assert mixed.heads_per_cta == 1 and mixed.box_tokens == 16 and mixed.stages >= 2
+    assert mixed.stage_bytes == (3 + 2) * 64 * 128
+    assert mixed.num_slots == 8 * 128 + mixed.num_ctas
+    wide = dict(num_q_heads=32, num_kv_heads=4, max_draft=5)           # 8 x 5 = 40 rows
+    assert _plan(page_size=64, **wide).path == va.VA_PATH_TC and _plan(page_size=64, **wide).box_tokens == 64
+    assert _plan(page_size=8, **wide).path == va.VA_PATH_TC and _plan(page_size=8, **wide).box_tokens == 8
+    mqa = dict(num_q_heads=32, num_kv_heads=1, max_draft=4, page_size=16)   # 32 x 4 = 128 rows
+    assert _plan(**mqa).rows_cap == 128 and _plan(**mqa).path == va.VA_PATH_TC
+    # 32 rows or fewer and other page sizes stay on the warp-level kernel
+    assert _plan(page_size=64).path == va.VA_PATH_MMA                     # 4 x 4 = 16 rows
+    assert _plan(page_size=64, num_q_heads=32, num_kv_heads=4, max_draft=4).path == va.VA_PATH_MMA
+    assert _plan(num_q_heads=32, num_kv_heads=1, max_draft=4).path == va.VA_PATH_MMA   # page size 4
+    # more than 128 rows per kv-head has no compiled kernel (8 m16 tiles at most)
+    with pytest.raises(va.VerifyAttnError):
+        _plan(num_q_heads=32, num_kv_heads=1, max_draft=5, page_size=16)
+    mma = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128,
+                page_size=4)
+    assert mma.path == va.VA_PATH_MMA and mma.variant == 3      # 40 rows -> 3 m16 tiles
+    assert mma.heads_per_cta == 2 and mma.box_tokens == 4       # 2 heads x 3 tiles = 6 warps
+    assert _plan(page_size=1).box_tokens == 1 and _plan(page_size=6).box_tokens == 2
+    assert _plan(page_size=12).path == va.VA_PATH_MMA            # gcd(12, 64) = 4 < 8
     assert _plan(num_ctas=7).num_ctas == 7
 
 

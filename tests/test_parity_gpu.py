@@ -105,18 +105,29 @@ def test_split_partition_invariance(num_ctas):
 
 
 def test_page_size_invariance():
-    """The same logical KV paged with page size 1, 4, 16 and 64 over different
+    """The same logical KV paged with page size 1, 4, 8, 16 and 64 over different
     random permutations ("Support Page Size > 1 (when top k = 1) for FA3 Spec
-    Decode": garbage output for page size > 1 was the bug). Tiles follow
-    absolute positions, so the kernels' results are bit-identical too."""
-    wl = small("llama8b_gqa", bs=4)
+    Decode": garbage output for page size > 1 was the bug). Every page size
+    matches the oracle; tiles follow absolute positions, so page sizes served
+    by the same kernel (1 and 4 by the warp-level one, multiples of 8 by the
+    tcgen05 one at 8 q-heads x 5 drafts = 40 rows per kv-head) give
+    bit-identical results."""
+    wl = small("llama8b_gqa", bs=4, num_q_heads=64, draft=("fixed", 5))
     lg = synth.make_logical(wl)
-    outs = []
-    for ps, seed in ((1, 3), (4, 5), (16, 8), (64, 9)):
+    by_path = {}
+    for ps, seed in ((1, 3), (4, 5), (8, 6), (16, 8), (64, 9)):
         pb = synth.paginate(lg, page_size=ps, seed=seed)
-        outs.append(check(pb))
-    for o, l in outs[1:]:
-        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+        plan = va.verify_attn_plan(max_bs=wl.bs, max_draft=int(pb.num_draft.max()),
+                                   num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                                   qk_dim=wl.qk_dim, v_dim=wl.v_dim, page_size=ps,
+                                   dtype=synth.DTYPE_CODES[wl.dtype], max_kv_len=4096,
+                                   num_pages=pb.num_pages,
+                                   num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+        by_path.setdefault(plan.path, []).append(check(pb))
+    assert len(by_path) == 2, sorted(by_path)
+    for outs in by_path.values():
+        for o, l in outs[1:]:
+            assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
