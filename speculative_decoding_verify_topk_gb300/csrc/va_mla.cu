@@ -29,8 +29,9 @@
 //     multicast, and a stage is refilled only after both ranks' MMAs have
 //     released it (MMA completion multicast to both).
 // Roles per CTA: warp 0 issues TMA; warp 1 issues the MMAs (one thread,
-// event-driven: P V of a tile as soon as its P is written, the scores of the
-// next tile as soon as its stage has landed, so they overlap the softmax);
+// event-driven: P V of a tile as soon as its P is written, which frees its KV
+// stage early -- with two stages the next load waits on it -- and the scores of
+// the next tile as soon as its stage has landed, so they overlap the softmax);
 // warps 2..5 (128 threads, thread = row) write the TMEM part of the query at
 // a segment start, read scores from TMEM, run the softmax, write P (bf16) to
 // shared memory, rescale O in TMEM when the running max moves by more than
@@ -47,10 +48,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include "va_common.cuh"
+#include "va_tc.cuh"
 
 namespace va {
 namespace {
+
+using namespace tc;
 
 constexpr int kTok = 64;          // tokens per tile (N of the score MMA, K of the PV MMA)
 constexpr int kRows = 128;        // rows per block (M of both MMAs)
@@ -63,9 +66,6 @@ constexpr int kQBytes = (kChunks - kQTmem) * kRows * 128;   // [chunk][128 rows]
 constexpr int kStageBytes = kChunks * kTok * 128;           // [chunk][64 tokens][128 B], 128-byte swizzle
 constexpr int kPBytes = kRows * kTok * 2;                   // P: [128 rows][128 B], 128-byte swizzle
 constexpr uint32_t kColS = 0, kColQ = 64, kColO = 256;      // TMEM columns
-// the MMA issuer's no-progress limit in SM cycles (about 2 s at 2 GHz, longer at lower clocks)
-constexpr long long kSpinCycles = 1LL << 32;
-
 struct MlaGeo {
     int stages;          // KV ring depth
     int tb;              // tokens per TMA box: gcd(page_size, 64)
@@ -82,37 +82,6 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// tcgen05 shared-memory matrix descriptor (sm_100 format: version 1 at bit 46,
-// layout type at bits 61..63: 0 = no swizzle, 2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
-}
-// instruction descriptor: bf16 x bf16 -> fp32, M x N, operand majors (0 = K, 1 = MN)
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
-// the same with the A operand in TMEM (rows = lanes, bf16 pairs per 32-bit column)
-__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
-// arrive on this CTA's barrier once the MMAs issued so far have completed
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
 // the same, arriving on the barrier at this offset in both CTAs of the pair
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
     asm volatile(
@@ -120,30 +89,6 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
         "h"((unsigned short)3)
         : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-
-#define VA_TMEM_LD32(taddr, r)                                                                       \
-    asm volatile(                                                                                    \
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"             \
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),       \
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),             \
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
-        : "r"(taddr))
-#define VA_TMEM_ST32(taddr, r)                                                                       \
-    asm volatile(                                                                                    \
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"  \
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr), \
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),     \
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),           \
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),         \
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),         \
-        "r"(r[29]), "r"(r[30]), "r"(r[31])                                                           \
-        : "memory")
-
 // 2-d TMA box into the same shared-memory offset of both CTAs of the pair;
 // each receiving CTA's barrier at `bar`'s offset counts the bytes
 __device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -152,23 +97,6 @@ __device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
         "l"(map), "r"(c0), "r"(c1), "r"(bar), "h"((unsigned short)3)
         : "memory");
-}
-
-// non-blocking: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // Partial-result slot of (row block rb, sequence b) written by cluster p.
@@ -226,9 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          smem_u32(&tmem_base)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
-    tc_fence_before();
+    fence_before();
     cluster_sync();   // both ranks' barriers and zeroed buffers exist before any multicast
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem = tmem_base;
     const uint32_t t_s = tmem + kColS, t_q = tmem + kColQ, t_o = tmem + kColO;
 
@@ -240,16 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t x_begin = cta_start(pair, work, geo.pairs);
     const int n_tiles = (int)(cta_start(pair + 1, work, geo.pairs) - x_begin);
 
-    // `site` numbers the wait; a wait that gives up records its bit in the
+    // `site` numbers a wait; a wait that gives up records its bit in the
     // header's wait-site word (diagnostics for VA_ERR_TIMEOUT)
-    auto wait_or_abort = [&](uint32_t bar, uint32_t parity, int site) {
-        if (*(volatile int*)&abort_flag) return;
-        if (!mbar_wait(bar, parity)) {
-            set_error(a, VA_ERR_TIMEOUT);
-            atomicOr(a.header + kHdrWaitSites, 1 << site);
-            abort_flag = 1;
-        }
-    };
+    int* const hdr = a.header;
 
     if (n_tiles > 0) {
         Cursor cur;
@@ -284,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (k == 0 || cur.t == 0) {
                         ++seg;
-                        if (seg >= 1) wait_or_abort(b_qfree, (seg - 1) & 1, 1);
+                        if (seg >= 1) wait_fast(b_qfree, (seg - 1) & 1, 1, &abort_flag, hdr);
                         const bool rows = cur.g < si.draft;   // this draft exists
                         mbar_arrive_expect_tx(b_qfull, rows ? (uint32_t)kQBytes : 0u);
                         if (rows) {
@@ -294,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             b_qfull);
                         }
                     }
-                    if (k >= geo.stages) wait_or_abort(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2);
+                    if (k >= geo.stages) wait_fast(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2, &abort_flag, hdr);
                     mbar_arrive_expect_tx(b_kfull + 8 * st, nbox * kChunks * geo.tb * 128);
                     unsigned char* const stg = ring + st * kStageBytes;
 #pragma unroll
@@ -318,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // place. The scores of tile k + 1 may start before P V of tile k,
             // so the tensor pipe works on them during tile k's softmax.
             if (lane == 0) {
-                const uint32_t id_s = idesc_bf16(kRows, kTok, 0, 0);
-                const uint32_t id_o = idesc_bf16(kRows, kV / 2, 0, 1);
+                const uint32_t id_s = idesc_f16(kRows, kTok, 0, 0, 1);
+                const uint32_t id_o = idesc_f16(kRows, kV / 2, 0, 1, 1);
                 // descriptors at offset 0; offsets (>> 4) add into the address field
                 const uint64_t q_desc = sdesc(smem_u32(qs), 16, 1024, 2);
                 const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
@@ -332,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
                         const int k = pv_next, st = k % geo.stages;
                         const bool first = (k == 0) || (pv_cur.t == 0);
-                        tc_fence_after();
+                        fence_after();
                         const uint64_t v_desc =
                             sdesc(smem_u32(ring + st * kStageBytes + rank * 4 * kTok * 128), kTok * 128, 1024, 2);
 #pragma unroll
@@ -355,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ready) {
                             const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
                             if (seg_begin) ++qk_seg;
-                            tc_fence_after();
+                            fence_after();
                             // S = Q K^T  (M 128, N 64, K 576 in 36 steps of 16)
                             const uint64_t k_desc = sdesc(smem_u32(ring + st * kStageBytes), 16, 1024, 2);
 #pragma unroll
@@ -388,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the peer's last commits land on this CTA's barriers: see them
                 // arrive before the CTA may exit
                 for (int k = n_tiles - geo.stages < 0 ? 0 : n_tiles - geo.stages; k < n_tiles; ++k)
-                    wait_or_abort(b_kempty + 8 * (k % geo.stages), (k / geo.stages) & 1, 12);
-                wait_or_abort(b_qfree, qk_seg & 1, 13);
+                    wait_fast(b_kempty + 8 * (k % geo.stages), (k / geo.stages) & 1, 12, &abort_flag, hdr);
+                wait_fast(b_qfree, qk_seg & 1, 13, &abort_flag, hdr);
             }
         } else {
             // =================== softmax warps: thread = row ===================
@@ -409,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++seg;
                     // 0. this row's query chunks 0..5 into TMEM once the previous
                     //    segment's score MMAs are done with them
-                    if (seg >= 1) wait_or_abort(b_qfree, (seg - 1) & 1, 0);
-                    tc_fence_after();
+                    if (seg >= 1) wait_fast(b_qfree, (seg - 1) & 1, 0, &abort_flag, hdr);
+                    fence_after();
                     const bool live = i < si.draft;
                     const uint4* qrow = reinterpret_cast<const uint4*>(
                         static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)(si.qoff + i) * a.hq + row) * kQk);
@@ -422,10 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint4 x = live ? __ldg(qrow + c * 8 + v) : make_uint4(0, 0, 0, 0);
                             r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
                         }
-                        VA_TMEM_ST32(t_q + c * 32 + lane_off, r);
+                        VA_TC_ST32(t_q + c * 32 + lane_off, r);
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-                    tc_fence_before();
+                    tmem_wait_st();
+                    fence_before();
                     mbar_arrive(b_qtmem);
                 }
                 // causal: keys up to P + i; tree verify: every prefix key and
@@ -437,73 +358,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool live_rows = i < si.draft;
                 const uint32_t tm = (a.tree && live_rows) ? __ldg(a.tree + si.qoff + i) : 0u;
 
-                // 1. scores from TMEM
-                wait_or_abort(b_sfull, k & 1, 7);
-                tc_fence_after();
-                float s[kTok];
-                {
-                    uint32_t r[32];
-                    VA_TMEM_LD32(t_s + lane_off, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]) * a.scale_log2;
-                    VA_TMEM_LD32(t_s + 32 + lane_off, r);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]) * a.scale_log2;
-                }
-                tc_fence_before();
+                // 1. scores from TMEM, one round trip (raw scores; the scale is
+                //    positive, so it commutes with max)
+                wait_fast(b_sfull, k & 1, 7, &abort_flag, hdr);
+                fence_after();
+                uint32_t r[kTok];
+                VA_TC_LD32(t_s + lane_off, r);
+                VA_TC_LD32(t_s + 32 + lane_off, (r + 32));
+                tmem_wait_ld();
+                fence_before();
                 mbar_arrive(b_sfree);
-                // 2. mask (the same for every row of the block) and online softmax
-                //    in base 2 with lazy rescaling by 2^8
+                // 2. mask (the same for every row of the block: invisible keys
+                //    -> -inf) and online softmax in base 2 with lazy rescaling by 2^8
                 if (!live_rows || j0 < lo || j0 + kTok - 1 > hi || (a.tree && j0 + kTok > si.prefix)) {
+                    uint64_t vis = 0ull;   // bit j: key j0 + j is visible
+                    if (live_rows) {
+                        const int vlo = lo - j0, vhi = hi - j0;
+                        if (vhi >= 0 && vlo <= kTok - 1 && vhi >= vlo) {
+                            vis = ~0ull;
+                            if (vhi < kTok - 1) vis &= (2ull << vhi) - 1ull;
+                            if (vlo > 0) vis &= ~((1ull << vlo) - 1ull);
+                        }
+                        if (a.tree) {
+                            // keys from P on are drafts: draft d needs bit d of the block's mask
+                            const int d0 = si.prefix - j0;   // tile column of draft 0
+                            if (d0 < kTok) {
+                                const uint64_t tb = d0 >= 0 ? (uint64_t)tm << d0 : (uint64_t)tm >> (-d0);
+                                const uint64_t before = d0 > 0 ? (1ull << d0) - 1ull : 0ull;
+                                vis &= before | tb;
+                            }
+                        }
+                    }
+                    const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
 #pragma unroll
-                    for (int j = 0; j < kTok; ++j) {
-                        const int t = j0 + j;
-                        if (!live_rows || t > hi || t < lo ||
-                            (a.tree && t >= si.prefix && !((tm >> (t - si.prefix)) & 1u)))
-                            s[j] = -INFINITY;
+                    for (int j = 0; j < 32; ++j) {
+                        r[j] = (v0 >> j) & 1u ? r[j] : 0xff800000u;
+                        r[32 + j] = (v1 >> j) & 1u ? r[32 + j] : 0xff800000u;
                     }
                 }
-                float mx[4] = {s[0], s[1], s[2], s[3]};
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 4; j < kTok; j += 4) {
-                    mx[0] = fmaxf(mx[0], s[j]);
-                    mx[1] = fmaxf(mx[1], s[j + 1]);
-                    mx[2] = fmaxf(mx[2], s[j + 2]);
-                    mx[3] = fmaxf(mx[3], s[j + 3]);
-                }
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                for (int j = 0; j < kTok; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(r[j]));
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const bool rescale = m_tile > m_ref + 8.f;
                 float alpha = 1.f;
                 if (rescale) {
-                    alpha = ex2_approx(m_ref - m_tile);   // 0 when m_ref is -inf
+                    alpha = ex2(m_ref - m_tile);   // 0 when m_ref is -inf
                     m_ref = m_tile;
                 }
                 const float mu = m_ref == -INFINITY ? 0.f : m_ref;
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) {
-                    s[j] = ex2_approx(s[j] - mu);
-                    ps4[j & 3] += s[j];
+                for (int j = 0; j < kTok; ++j) {   // -inf (an invisible key) gives exactly 0
+                    const float x = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -mu));
+                    ps4[j & 3] += x;
+                    r[j] = __float_as_uint(x);
                 }
                 l_sum = l_sum * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
                 // 3. the previous P V must be done before P is rewritten or O rescaled
-                if (k >= 1) wait_or_abort(b_pvdone, (k - 1) & 1, 10);
-                tc_fence_after();
+                if (k >= 1) wait_fast(b_pvdone, (k - 1) & 1, 10, &abort_flag, hdr);
+                fence_after();
                 // tcgen05.ld / st are warp-collective: the warp rescales if any of
                 // its rows needs it (the others multiply by alpha = 1)
                 if (__any_sync(0xffffffffu, rescale) && !seg_begin) {
                     uint32_t r[32];
 #pragma unroll 1
                     for (int c = 0; c < kV / 2; c += 32) {
-                        VA_TMEM_LD32(t_o + c + lane_off, r);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                        VA_TC_LD32(t_o + c + lane_off, r);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                        VA_TMEM_ST32(t_o + c + lane_off, r);
+                        VA_TC_ST32(t_o + c + lane_off, r);
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                    tmem_wait_st();
                 }
                 // V rows of tokens past the sequence end may hold garbage: zero
                 // this rank's V chunks there (0 * NaN would poison P V)
@@ -526,26 +453,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(s[q * 8 + 2 * e], s[q * 8 + 2 * e + 1]);
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[q * 8 + 2 * e]),
+                                                                  __uint_as_float(r[q * 8 + 2 * e + 1]));
                         w[e] = *reinterpret_cast<uint32_t*>(&h2);
                     }
                     *reinterpret_cast<uint4*>(ps + row * 128 + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 fence_proxy_async_smem();
-                tc_fence_before();
+                fence_before();
                 mbar_arrive(b_pfull);
                 // 5. segment end: normalised partial output of this rank's v half
                 if (seg_end) {
-                    wait_or_abort(b_pvdone, k & 1, 11);
-                    tc_fence_after();
+                    wait_fast(b_pvdone, k & 1, 11, &abort_flag, hdr);
+                    fence_after();
                     const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;   // times the V dequant scale
                     const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
                     float* po = a.part_o + (slot * kRows + row) * kV + rank * (kV / 2);
                     uint32_t r[32];
 #pragma unroll 1
                     for (int c = 0; c < kV / 2; c += 32) {
-                        VA_TMEM_LD32(t_o + c + lane_off, r);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                        VA_TC_LD32(t_o + c + lane_off, r);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<float4*>(po + c + j) =
@@ -554,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (rank == 0)
                         a.part_lse[slot * kRows + row] = l_sum > 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
-                    tc_fence_before();
+                    fence_before();
                 }
                 if (k + 1 < n_tiles) cur.advance(a);
             }
@@ -562,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // teardown: every MMA of this CTA has been waited on (pv_done of its last
     // tile), and the peer's multicast commits to this CTA have arrived
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     cluster_sync();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));

@@ -20,9 +20,9 @@
 //   * S (128 x 64 fp32) lives in TMEM, double-buffered; O (128 x Dv fp32) too;
 //     P (bf16 / fp16) goes through shared memory as the A operand of P V, with V
 //     token-major (MN-major B);
-//   * warp 2 issues TMA, warp 3 the MMAs (one thread, event-driven: P V of a
-//     tile as soon as its P is written, the next tile's scores as soon as their
-//     stage has landed), warps 4..7 run the online softmax (thread = row) with
+//   * warp 2 issues TMA, warp 3 the MMAs (one thread, a fixed pipeline: the
+//     scores of tile k + 1, then P V of tile k), warps 4..7 run the online
+//     softmax (thread = row) with
 //     lazy rescaling of O in TMEM (only when a row's max grows by more than
 //     2^8) and write the segment's partial output.
 // Compared with the warp-level kernel, the contraction runs on the tcgen05
@@ -81,24 +81,6 @@ __device__ __forceinline__ uint32_t pack2(float x, float y) {
         __half2 h = __floats2half2_rn(x, y);
         return *reinterpret_cast<uint32_t*>(&h);
     }
-}
-
-// Bounded wait shared by every waiter of the kernel, one copy of the spin
-// loop for all call sites (the loop sits on the instruction stream of every
-// waiting warp). After a timeout it flags VA_ERR_TIMEOUT with the wait site
-// and raises the CTA's abort flag; once the flag is up nobody waits again.
-__device__ __noinline__ void wait_or_abort(uint32_t bar, uint32_t parity, int site, int* abort_flag, int* header) {
-    if (*(volatile int*)abort_flag) return;
-    if (!mbar_wait(bar, parity)) {
-        atomicOr(header + kHdrError, VA_ERR_TIMEOUT);
-        atomicOr(header + kHdrWaitSites, 1 << site);
-        *(volatile int*)abort_flag = 1;
-    }
-}
-
-// The common case -- the phase has already completed -- stays inline.
-__device__ __forceinline__ void wait_fast(uint32_t bar, uint32_t parity, int site, int* abort_flag, int* header) {
-    if (!mbar_try_wait(bar, parity)) wait_or_abort(bar, parity, site, abort_flag, header);
 }
 
 template <typename T, int DQK, int DV>
@@ -249,11 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (seg_end) umma_commit(b_qfree);   // the segment's query is no longer read
                     if (k + 1 < n_tiles) qk_cur.advance(a);
                 };
-                issue_qk(0);
-                for (int k = 0; k < n_tiles; ++k) {
-                    const bool next = k + 1 < n_tiles;
-                    const bool next_opens = next && qk_cur.t == 0;   // qk_cur sits on tile k + 1
-                    if (next && !next_opens) issue_qk(k + 1);
+                // One action per pass: the scores of tile q (q <= k + 1) unless q
+                // is the next tile and opens a segment, else P V of tile k.
+                int q = 0;
+                for (int k = 0; k < n_tiles;) {
+                    if (q < n_tiles && q <= k + 1 && (q == k || qk_cur.t != 0)) {
+                        issue_qk(q++);
+                        continue;
+                    }
                     // O += P V  (M 128, N Dv, K 64 tokens; V token-major)
                     const int st = k % geo.stages;
                     const bool first = (k == 0) || (pv_cur.t == 0);
@@ -268,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              !(first && s4 == 0));
                     umma_commit(b_pvdone + 8 * (k & 1));
                     umma_commit(b_kempty + 8 * st);
-                    if (next) pv_cur.advance(a);
-                    if (next_opens) issue_qk(k + 1);
+                    if (k + 1 < n_tiles) pv_cur.advance(a);
+                    ++k;
                 }
                 // the last commits have landed before the CTA may exit
                 wait_fast(b_pvdone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, 12, &abort_flag, hdr);

@@ -122,8 +122,27 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// the MMA issuer's no-progress limit in SM cycles (about 2 s at 2 GHz, longer at lower clocks)
+// an event-driven MMA issuer's no-progress limit in SM cycles (about 2 s at
+// 2 GHz, longer at lower clocks)
 constexpr long long kSpinCycles = 1LL << 32;
+
+// Bounded wait shared by every waiter of a kernel, one copy of the spin loop
+// for all call sites (the loop sits on the instruction stream of every
+// waiting warp). After a timeout it flags VA_ERR_TIMEOUT with the wait site
+// and raises the CTA's abort flag; once the flag is up nobody waits again.
+static __device__ __noinline__ void wait_or_abort(uint32_t bar, uint32_t parity, int site, int* abort_flag,
+                                                  int* header) {
+    if (*(volatile int*)abort_flag) return;
+    if (!mbar_wait(bar, parity)) {
+        atomicOr(header + kHdrError, VA_ERR_TIMEOUT);
+        atomicOr(header + kHdrWaitSites, 1 << site);
+        *(volatile int*)abort_flag = 1;
+    }
+}
+// The common case -- the phase has already completed -- stays inline.
+__device__ __forceinline__ void wait_fast(uint32_t bar, uint32_t parity, int site, int* abort_flag, int* header) {
+    if (!mbar_try_wait(bar, parity)) wait_or_abort(bar, parity, site, abort_flag, header);
+}
 
 }  // namespace tc
 }  // namespace va
