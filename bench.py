@@ -49,7 +49,7 @@ FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {  # files whose change invalidates a stored ncu traffic figure
     "prefix_mma": ["va_prefix_mma.cuh", "va_common.cuh"],
     "prefix_f32": ["va_prefix_f32.cu", "va_common.cuh"],
-    "prefix_mla": ["va_mla.cu", "va_common.cuh"],
+    "prefix_mla": ["va_mla.cu", "va_tc.cuh", "va_common.cuh"],
     "prefix_tc": ["va_prefix_tc.cu", "va_tc.cuh", "va_common.cuh"],
 }
 
