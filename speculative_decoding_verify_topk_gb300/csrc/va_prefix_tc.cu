@@ -147,54 +147,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur.seek(a, x_begin, total_tiles);   // cur.g = kv-head
 
         if (warp == kProducerWarp) {
-            // =================== TMA producer (one thread) ===================
-            if (lane == 0) {
-                const int tb_log2 = __ffs(geo.tb) - 1;   // boxes are 2^tb_log2 tokens
-                const uint32_t box_bytes = (uint32_t)(L::kQc + L::kVc) * geo.tb * 128;
-                int b_seen = -1, indptr = 0;
-                SeqInfo si = {};
-                for (int k = 0; k < n_tiles; ++k) {
-                    const int st = k % geo.stages;
-                    if (cur.b != b_seen) {
-                        si = a.seq[cur.b];
-                        indptr = __ldg(a.kv_indptr + cur.b);
-                        b_seen = cur.b;
-                    }
-                    // the boxes [q0, q1) of the tile that overlap the keys [lo, P + D)
-                    const int j0 = si.a0 + cur.t * kTok;
-                    const int end = si.prefix + si.draft;
-                    const int q0 = si.lo > j0 ? (si.lo - j0) >> tb_log2 : 0;
-                    int q1 = end < j0 + kTok ? (end - j0 + geo.tb - 1) >> tb_log2 : kTok >> tb_log2;
-                    if (q1 < q0) q1 = q0;
+            // =================== TMA producer (one warp) ===================
+            // Lane 0 waits for the stage and posts the byte count; then lane q
+            // resolves the page of the tile's box q0 + q and issues its copies,
+            // so the boxes of a tile go out in parallel.
+            const int tb_log2 = __ffs(geo.tb) - 1;   // boxes are 2^tb_log2 tokens
+            const uint32_t box_bytes = (uint32_t)(L::kQc + L::kVc) * geo.tb * 128;
+            int b_seen = -1, indptr = 0;
+            SeqInfo si = {};
+            for (int k = 0; k < n_tiles; ++k) {
+                const int st = k % geo.stages;
+                if (cur.b != b_seen) {
+                    si = a.seq[cur.b];
+                    indptr = __ldg(a.kv_indptr + cur.b);
+                    b_seen = cur.b;
+                }
+                // the boxes [q0, q1) of the tile that overlap the keys [lo, P + D)
+                const int j0 = si.a0 + cur.t * kTok;
+                const int end = si.prefix + si.draft;
+                const int q0 = si.lo > j0 ? (si.lo - j0) >> tb_log2 : 0;
+                int q1 = end < j0 + kTok ? (end - j0 + geo.tb - 1) >> tb_log2 : kTok >> tb_log2;
+                if (q1 < q0) q1 = q0;
+                if (lane == 0) {
                     if (k >= geo.stages)
                         wait_fast(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2, &abort_flag, hdr);
                     mbar_arrive_expect_tx(b_kfull + 8 * st, (uint32_t)(q1 - q0) * box_bytes);
+                }
+                __syncwarp();
+                const int q = q0 + lane;
+                if (q < q1) {
                     const uint32_t stg = smem_u32(ring + st * geo.stage_bytes);
-#pragma unroll 1
-                    for (int q = q0; q < q1; ++q) {
-                        const int j = j0 + (q << tb_log2);
-                        const int page = __ldg(a.page_table + indptr + j / a.page_size);
-                        if (page < 0 || page >= a.num_pages) set_error(a, VA_ERR_BAD_PAGE);
-                        // an out-of-range id still delivers its bytes (from page 0) so the count balances
-                        const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size + j % a.page_size;
-                        const uint32_t dst = stg + (uint32_t)(q << tb_log2) * 128;
+                    const int j = j0 + (q << tb_log2);
+                    const int page = __ldg(a.page_table + indptr + j / a.page_size);
+                    if (page < 0 || page >= a.num_pages) set_error(a, VA_ERR_BAD_PAGE);
+                    // an out-of-range id still delivers its bytes (from page 0) so the count balances
+                    const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size + j % a.page_size;
+                    const uint32_t dst = stg + (uint32_t)(q << tb_log2) * 128;
 #pragma unroll
-                        for (int c = 0; c < L::kQc; ++c)
-                            tma_3d(dst + c * kChunkBytes, &kmap, c * 64, slot, cur.g, b_kfull + 8 * st);
+                    for (int c = 0; c < L::kQc; ++c)
+                        tma_3d(dst + c * kChunkBytes, &kmap, c * 64, slot, cur.g, b_kfull + 8 * st);
 #pragma unroll
-                        for (int c = 0; c < L::kVc; ++c)
-                            tma_3d(dst + (L::kQc + c) * kChunkBytes, &vmap, c * 64, slot, cur.g, b_kfull + 8 * st);
-                    }
-                    // the combine may launch while this CTA drains its ring
-                    if (k + 1 == n_tiles) pdl_launch_dependents();
-                    if (k + 1 < n_tiles) cur.advance(a);
+                    for (int c = 0; c < L::kVc; ++c)
+                        tma_3d(dst + (L::kQc + c) * kChunkBytes, &vmap, c * 64, slot, cur.g, b_kfull + 8 * st);
                 }
-                // Normally the MMAs consume every fill before the CTA ends. After
-                // an abort, wait (bounded) for the last fill of each stage.
-                if (*(volatile int*)&abort_flag) {
-                    const int k0 = n_tiles - geo.stages > 0 ? n_tiles - geo.stages : 0;
-                    for (int k = k0; k < n_tiles; ++k) mbar_wait(b_kfull + 8 * (k % geo.stages), (k / geo.stages) & 1);
-                }
+                // the combine may launch while this CTA drains its ring
+                if (k + 1 == n_tiles && lane == 0) pdl_launch_dependents();
+                if (k + 1 < n_tiles) cur.advance(a);
+            }
+            // Normally the MMAs consume every fill before the CTA ends. After an
+            // abort, wait (bounded) for the last fill of each stage.
+            if (lane == 0 && *(volatile int*)&abort_flag) {
+                const int k0 = n_tiles - geo.stages > 0 ? n_tiles - geo.stages : 0;
+                for (int k = k0; k < n_tiles; ++k) mbar_wait(b_kfull + 8 * (k % geo.stages), (k / geo.stages) & 1);
             }
         } else if (warp == kMmaWarp) {
             // =================== MMA issuer (one thread) ===================
