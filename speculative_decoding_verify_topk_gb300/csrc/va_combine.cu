@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "va_common.cuh"
 
 namespace va {
@@ -50,6 +52,38 @@ __device__ __forceinline__ void load_f32(const float* p, float (&v)[VPL]) {
         for (int e = 0; e < VPL; e += 2) {
             const float2 x = *reinterpret_cast<const float2*>(p + e);
             v[e] = x.x; v[e + 1] = x.y;
+        }
+    }
+}
+
+// The lane's VPL outputs (times inv) as vector stores: VPL elements start at
+// a multiple of VPL, so 16-bit outputs go out as 4-, 8- or 16-byte words.
+template <typename T, int VPL>
+__device__ __forceinline__ void store_row(T* og, const float (&acc)[VPL], float inv) {
+    if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+        for (int e = 0; e < VPL; e += 2)
+            *reinterpret_cast<float2*>(og + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+    } else {
+        uint32_t w[VPL / 2];
+#pragma unroll
+        for (int e = 0; e < VPL; e += 2) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+                w[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+                const __half2 h = __floats2half2_rn(acc[e] * inv, acc[e + 1] * inv);
+                w[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+        }
+        if constexpr (VPL % 8 == 0) {
+#pragma unroll
+            for (int e = 0; e < VPL / 2; e += 4)
+                *reinterpret_cast<uint4*>(og + 2 * e) = make_uint4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+        } else if constexpr (VPL == 4) {
+            *reinterpret_cast<uint2*>(og) = make_uint2(w[0], w[1]);
+        } else {
+            *reinterpret_cast<uint32_t*>(og) = w[0];
         }
     }
 }
@@ -103,9 +137,13 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     const int c_first = cta_of_tile(x0, work, workers);
     const int c_last = cta_of_tile(x0 + si.tiles - 1, work, workers);
     const bool all_busy = work >= workers;   // then every worker got at least one tile
-    auto live = [&](int c) {   // worker c covered some tile (more workers than tiles leaves some idle)
-        return c <= c_last &&
-               (all_busy || cta_start(c + 1, work, workers) != cta_start(c, work, workers));
+    // Whether worker c covered some tile (more workers than tiles leaves some
+    // idle). Each lane evaluates it for one worker of a run of 32 and the warp
+    // shares the answers as a ballot word, so the division sits in the code once.
+    auto live_word = [&](int cb) {
+        const int c = cb + lane;
+        const bool live = c <= c_last && (all_busy || cta_start(c + 1, work, workers) != cta_start(c, work, workers));
+        return __ballot_sync(0xffffffffu, live);
     };
 
     // ---- one round of independent loads: the segments' lse values (lane c
@@ -115,15 +153,19 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     auto row_ptr = [&](int c) {
         return a.part_o + ((slot0 + c) * slot_rows + prow) * (VPL * 32) + lane * VPL;
     };
-    const float lse_first = live(c_first + lane) ? a.part_lse[(slot0 + c_first + lane) * slot_rows + prow]
-                                                 : -INFINITY;
+    const uint32_t live0 = live_word(c_first);
+    const float lse_first =
+        (live0 >> lane) & 1u ? a.part_lse[(slot0 + c_first + lane) * slot_rows + prow] : -INFINITY;
     float v[kBatch][VPL];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u)
-        if (live(c_first + u)) load_f32<VPL>(row_ptr(c_first + u), v[u]);
+        if ((live0 >> u) & 1u) load_f32<VPL>(row_ptr(c_first + u), v[u]);
     float mx = lse_first;
-    for (int c = c_first + 32 + lane; c <= c_last; c += 32)   // more than 32 segments: rare
-        if (live(c)) mx = fmaxf(mx, a.part_lse[(slot0 + c) * slot_rows + prow]);
+#pragma unroll 1
+    for (int cb = c_first + 32; cb <= c_last; cb += 32) {   // more than 32 segments: rare
+        const uint32_t lw = live_word(cb);
+        if ((lw >> lane) & 1u) mx = fmaxf(mx, a.part_lse[(slot0 + cb + lane) * slot_rows + prow]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
@@ -132,25 +174,26 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
 #pragma unroll
     for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
     float z = 0.f;   // lane-partial sum of weights
+#pragma unroll 1
     for (int cb = c_first; cb <= c_last; cb += 32) {
-        const int c = cb + lane;
+        const uint32_t lw = cb == c_first ? live0 : live_word(cb);
         float w = 0.f;
-        if (live(c)) {
-            const float lc = cb == c_first ? lse_first : a.part_lse[(slot0 + c) * slot_rows + prow];
+        if ((lw >> lane) & 1u) {
+            const float lc = cb == c_first ? lse_first : a.part_lse[(slot0 + cb + lane) * slot_rows + prow];
             w = lc == -INFINITY ? 0.f : exp2f(lc - mx);
         }
         z += w;
-        const int n = c_last - cb + 1 < 32 ? c_last - cb + 1 : 32;
-        for (int j = 0; j < n; j += kBatch) {
+#pragma unroll 1
+        for (int j = 0; j < 32 && (lw >> j) != 0u; j += kBatch) {
             if (cb != c_first || j != 0) {   // the first batch is already in registers
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u)
-                    if (j + u < n && live(cb + j + u)) load_f32<VPL>(row_ptr(cb + j + u), v[u]);
+                    if ((lw >> (j + u)) & 1u) load_f32<VPL>(row_ptr(cb + j + u), v[u]);
             }
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const float wj = __shfl_sync(0xffffffffu, w, (j + u) & 31);
-                if (j + u < n && wj != 0.f) {
+                if (((lw >> (j + u)) & 1u) && wj != 0.f) {
 #pragma unroll
                     for (int e = 0; e < VPL; ++e) acc[e] = fmaf(wj, v[u][e], acc[e]);
                 }
@@ -159,9 +202,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    const float inv = 1.f / z;
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) og[e] = from_f32<T>(acc[e] * inv);
+    store_row<T, VPL>(og, acc, 1.f / z);
     if (lane == 0) a.lse[qrow] = (mx + __log2f(z)) * 0.69314718055994531f;
 }
 
