@@ -182,14 +182,24 @@ struct Cursor {
     int g, b, t;
     int tiles;   // tiles of sequence b
     __device__ __forceinline__ void load_seq(const Args& a) { tiles = a.seq[b].tiles; }
-    // Positions the cursor at stream tile x (x < H * T).
+    // Positions the cursor at stream tile x (x < H * T). Warp-cooperative: all
+    // 32 lanes call it; each round probes 32 evenly spaced sequences in one
+    // load, so bs <= 32 takes one round of loads and bs <= 1024 two.
     __device__ __forceinline__ void seek(const Args& a, int64_t x, int total_tiles) {
+        const int lane = threadIdx.x & 31;
         g = (int)(x / total_tiles);
-        int rem = (int)(x - (int64_t)g * total_tiles);
-        int lo = 0, hi = a.bs - 1;        // largest b with tile_off_b <= rem
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (a.seq[mid].tile_off <= rem) lo = mid; else hi = mid - 1;
+        const int rem = (int)(x - (int64_t)g * total_tiles);
+        // the answer, the largest b with tile_off_b <= rem, lies in [lo, hi);
+        // tile_off_lo <= rem holds throughout (tile_off_0 = 0)
+        int lo = 0, hi = a.bs;
+        while (hi - lo > 1) {
+            const int step = (hi - lo + 31) >> 5;
+            const int probe = lo + lane * step;
+            const bool le = probe < hi && a.seq[probe].tile_off <= rem;
+            // tile offsets do not decrease, so the lanes that pass form a prefix
+            const uint32_t m = __ballot_sync(0xffffffffu, le);
+            lo += (31 - __clz(m)) * step;
+            hi = min(hi, lo + step);
         }
         b = lo;
         t = rem - a.seq[b].tile_off;
