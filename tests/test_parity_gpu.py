@@ -86,6 +86,20 @@ def test_tiny_fp32():
     check(synth.make_batch("tiny"))
 
 
+@pytest.mark.parametrize("bs", [33, 100, 1100])
+def test_many_sequences_gqa(bs):
+    """More than 32 sequences: a CTA's search for the sequence of its first
+    tile takes two rounds of 32 probes (bs <= 1024) or three, and most CTAs
+    start mid-stream among short, ragged sequences (some with empty prefixes)."""
+    wl = small("llama8b_gqa", bs=bs, prefix=("uniform", 0, 60), draft=("choice", [1, 2, 3]))
+    check(synth.make_batch(wl))
+
+
+def test_many_sequences_mla_and_fp32():
+    check(synth.make_batch(small("dsv3_mla", bs=40, prefix=("uniform", 0, 200))))
+    check(synth.make_batch("tiny", bs=40, prefix=("uniform", 0, 90), pool_tokens=None))
+
+
 @pytest.mark.parametrize("name", ["llama8b_gqa", "long_context"])
 def test_gqa_bf16_small(name):
     check(synth.make_batch(small(name)))

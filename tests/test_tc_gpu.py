@@ -91,6 +91,11 @@ def test_ragged_and_empty_prefixes():
     check(synth.paginate(lg, page_size=16, seed=4), max_draft=5)
 
 
+def test_many_sequences():
+    """100 sequences: a CTA's search for its first sequence takes two rounds."""
+    check(synth.make_batch(wide(bs=100, prefix=("uniform", 0, 200))))
+
+
 @pytest.mark.parametrize("num_ctas", [1, 7, 300])
 def test_partition_invariance(num_ctas):
     """One CTA (no split), a few, and more CTAs than the stream has tiles."""
