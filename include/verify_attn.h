@@ -336,6 +336,23 @@ int verify_attn_build_page_table(int bs, int page_size, int64_t num_pages,
                                  int32_t *page_table, int64_t capacity, int row_stride,
                                  int32_t *seq_lens, int32_t *error_word, void *stream);
 
+/*
+ * Diagnostics for failure detection: makes one bounded wait run out on the
+ * GPU, on purpose and without a fault. One CTA waits, twice, through the
+ * library's bounded mbarrier wait on a barrier that nothing arrives on. The
+ * first wait gives up after its 2 s wall-time limit. It ORs VA_ERR_TIMEOUT into
+ * header[0] and the wait-site bit (1 << 14) into header[3], and raises the
+ * CTA's abort flag. The second wait then returns at once (the wind-down that
+ * every kernel follows after a timeout).
+ *
+ * header:     device int32[4], caller-zeroed (the same word layout as a plan
+ *             workspace's header: error word, -, -, wait-site word).
+ * elapsed_ns: device int64[2]; receives the wall time of each wait.
+ * stream:     cudaStream_t (NULL = default stream); asynchronous, about 2 s.
+ * Returns VA_OK, VA_INVALID_ARG (a NULL pointer) or VA_CUDA_ERROR (launch).
+ */
+int verify_attn_selftest_timeout(int32_t *header, int64_t *elapsed_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ from .binding import (  # noqa: F401
     EXPORTS, LIB_PATH, Plan, Problem, VerifyAttnError, load_library, status_string,
     verify_attn_build_page_table, verify_attn_check, verify_attn_launches_per_call,
     verify_attn_paged, verify_attn_paged_scaled, verify_attn_paged_tree, verify_attn_plan,
+    verify_attn_selftest_timeout,
     VA_BF16, VA_FP16, VA_FP32, VA_FP8_E4M3, VA_PATH_F32, VA_PATH_MLA, VA_PATH_MMA, VA_PATH_TC,
-    VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE,
+    VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_TIMEOUT,
 )
 from .api import VerifyAttention, dtype_code  # noqa: F401

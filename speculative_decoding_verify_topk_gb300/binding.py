@@ -21,7 +21,7 @@ VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
            "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table",
-           "verify_attn_paged_tree", "verify_attn_paged_scaled")
+           "verify_attn_paged_tree", "verify_attn_paged_scaled", "verify_attn_selftest_timeout")
 
 
 class Problem(ctypes.Structure):
@@ -99,6 +99,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         L = ctypes.c_int64
         lib.verify_attn_build_page_table.argtypes = [I, I, L, P, P, P, P, P, L, I, P, P, P]
         lib.verify_attn_build_page_table.restype = I
+        lib.verify_attn_selftest_timeout.argtypes = [P, P, P]
+        lib.verify_attn_selftest_timeout.restype = I
         _lib = lib
         return lib
 
@@ -171,6 +173,17 @@ def verify_attn_check(plan: Plan, workspace, stream=None) -> int:
 
 def verify_attn_launches_per_call(plan: Plan) -> int:
     return load_library().verify_attn_launches_per_call(ctypes.byref(plan))
+
+
+def verify_attn_selftest_timeout(header, elapsed_ns, stream=None) -> None:
+    """Calls verify_attn_selftest_timeout: one bounded wait on the GPU runs out
+    on purpose (about 2 s). header: int32 device tensor of 4 zeros (word 0 gets
+    VA_ERR_TIMEOUT, word 3 the wait-site bit); elapsed_ns: int64 device tensor of
+    2 (each wait's wall time). Asynchronous; raises VerifyAttnError on a nonzero
+    status."""
+    rc = load_library().verify_attn_selftest_timeout(_ptr(header), _ptr(elapsed_ns), _stream_handle(stream))
+    if rc != VA_OK:
+        raise VerifyAttnError(rc, "verify_attn_selftest_timeout")
 
 
 def verify_attn_build_page_table(bs: int, page_size: int, num_pages: int, kv_indptr_tok, kv_indices,
