@@ -20,16 +20,17 @@
 //   * S (128 x 64 fp32) lives in TMEM, double-buffered; O (128 x Dv fp32) too;
 //     P (bf16 / fp16) goes through shared memory as the A operand of P V, with V
 //     token-major (MN-major B);
-//   * warp 2 issues TMA, warp 3 the MMAs (one thread, a fixed pipeline: the
-//     scores of tile k + 1, then P V of tile k), warps 4..7 run the online
-//     softmax (thread = row) with
-//     lazy rescaling of O in TMEM (only when a row's max grows by more than
-//     2^8) and write the segment's partial output.
+//   * warp 2 loads (lane q issues the copies of the tile's box q), warp 3
+//     issues the MMAs (one thread, a fixed pipeline: the scores of tile k + 1,
+//     then P V of tile k), warps 4..7 run the online softmax (thread = row)
+//     with lazy rescaling of O in TMEM (only when a row's max grows by more
+//     than 2^8) and write the segment's partial output.
 // Compared with the warp-level kernel, the contraction runs on the tcgen05
 // pipe (about four times the legacy mma throughput) and no warp holds the
-// accumulator in registers, so query-row counts up to 128 per kv-head (G * D:
-// e.g. 8 q-heads x 5 drafts) keep the path bandwidth-bound. Every wait is
-// bounded (VA_ERR_TIMEOUT, then the kernel winds down without waiting).
+// accumulator in registers. The plan takes this kernel for 33..128 query rows
+// per kv-head (G * D: e.g. 8 q-heads x 5 drafts), where the warp-level kernel
+// needs three or more m16 tiles per head. Every wait is bounded
+// (VA_ERR_TIMEOUT, then the kernel winds down without waiting).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

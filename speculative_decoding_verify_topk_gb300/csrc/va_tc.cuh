@@ -72,15 +72,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t cols) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
         : "r"(taddr))
-// 32 lanes x 16 consecutive 32-bit columns
-#define VA_TC_LD16(taddr, r)                                                                           \
-    asm volatile(                                                                                      \
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"  \
-        "%15}, [%16];\n"                                                                               \
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),     \
-          "=r"(r[14]), "=r"(r[15])                                                                    \
-        : "r"(taddr))
 #define VA_TC_ST32(taddr, r)                                                                         \
     asm volatile(                                                                                    \
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"  \
