@@ -12,8 +12,9 @@
 //
 // GB300 mapping (one CTA per SM, persistent, one kv-head per CTA at a time):
 //   * the head's query rows, padded with zero rows to M = 128, are the A
-//     operand of S = Q K^T in shared memory (K-major, 128-byte swizzle),
-//     written by the softmax threads at a segment start;
+//     operand of S = Q K^T in tensor memory (lane = row, 16-bit pairs per
+//     32-bit column), written by the softmax threads at a segment start;
+//     shared memory holds only the KV ring and P;
 //   * a tile is 64 tokens; its K and V rows arrive by TMA boxes of
 //     gcd(page_size, 64) tokens x 64 columns of the head (whole 1 KB swizzle
 //     atoms, so page sizes must be multiples of 8) into a ring of stages;
@@ -67,10 +68,11 @@ struct TcGeo {
 template <int DQK, int DV>
 struct Layout {
     static constexpr int kQc = DQK / 64, kVc = DV / 64;
-    static constexpr int kQBytes = kQc * kRows * 128;        // [chunk][128 rows][128 B]
     static constexpr int kPBytes = kRows * 128;               // [128 rows][64 tokens] 16-bit
-    static constexpr uint32_t kColS = 0, kColO = 2 * kTok;    // TMEM: S double-buffered, then O
-    static constexpr uint32_t kTmemCols = (kColO + DV) <= 256 ? 256 : 512;
+    // TMEM columns: S double-buffered, O, then the query (two 16-bit values a column)
+    static constexpr uint32_t kColS = 0, kColO = 2 * kTok, kColQ = kColO + DV;
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kColQ + DQK / 2 <= kTmemCols, "S, O and the query must fit in TMEM");
 };
 
 template <typename T>
@@ -91,8 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Layout<DQK, DV>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char* const qs = base;
-    unsigned char* const ring = qs + L::kQBytes;
+    unsigned char* const ring = base;
     unsigned char* const ps = ring + geo.stages * geo.stage_bytes;   // [2] P buffers
     uint64_t* const bars = reinterpret_cast<uint64_t*>(ps + 2 * L::kPBytes);
     const uint32_t b_kfull = smem_u32(bars);                 // [stages] producer arrive + tx
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t t_s = tmem + L::kColS, t_o = tmem + L::kColO;
+    const uint32_t t_s = tmem + L::kColS, t_o = tmem + L::kColO, t_q = tmem + L::kColQ;
 
     pdl_wait();
     const int total_tiles = a.header[kHdrTotalTiles];
@@ -212,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
                 const uint32_t id_s = idesc_f16(kRows, kTok, 0, 0, kBf16);
                 const uint32_t id_o = idesc_f16(kRows, DV, 0, 1, kBf16);
-                const uint64_t q_desc = sdesc(smem_u32(qs), 16, 1024, 2);
                 const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
                 Cursor qk_cur = cur, pv_cur = cur;
                 int qk_seg = -1;
@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < L::kQc; ++c)
 #pragma unroll
                         for (int s4 = 0; s4 < 4; ++s4)
-                            umma(t_s + sb * kTok, q_desc + (uint64_t)((c * kRows * 128 + s4 * 32) >> 4),
-                                 k_desc + (uint64_t)((c * kChunkBytes + s4 * 32) >> 4), id_s, (c | s4) != 0);
+                            umma_ts(t_s + sb * kTok, t_q + c * 32 + s4 * 8,
+                                    k_desc + (uint64_t)((c * kChunkBytes + s4 * 32) >> 4), id_s, (c | s4) != 0);
                     umma_commit(b_sfull + 8 * sb);
                     if (seg_end) umma_commit(b_qfree);   // the segment's query is no longer read
                     if (k + 1 < n_tiles) qk_cur.advance(a);
@@ -300,20 +300,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the query rows are zero (their scores are zero), rows of a
                     // dead warp keep stale values (their scores are never read)
                     if (seg >= 1) wait_fast(b_qfree, (seg - 1) & 1, 0, &abort_flag, hdr);
-                    if (wlive) {
+                    fence_after();
+                    if (wlive) {   // warp-uniform: tcgen05.st is warp-collective
                         const uint4* qrow = reinterpret_cast<const uint4*>(
                             static_cast<const T*>(a.q) + ((int64_t)(si.qoff + i) * a.hq + g * a.group + hh) * DQK);
 #pragma unroll 1
-                        for (int c = 0; c < L::kQc; ++c) {
-                            uint4 x[8];
+                        for (int c = 0; c < L::kQc; ++c) {   // 64 columns of the head = 32 TMEM columns
+                            uint32_t r[32];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) x[q] = rows_live ? __ldg(qrow + c * 8 + q) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                *reinterpret_cast<uint4*>(qs + c * kRows * 128 + row * 128 + ((q ^ (row & 7)) << 4)) = x[q];
+                            for (int q = 0; q < 8; ++q) {
+                                const uint4 x = rows_live ? __ldg(qrow + c * 8 + q) : make_uint4(0, 0, 0, 0);
+                                r[4 * q] = x.x;
+                                r[4 * q + 1] = x.y;
+                                r[4 * q + 2] = x.z;
+                                r[4 * q + 3] = x.w;
+                            }
+                            VA_TC_ST32(t_q + c * 32 + lane_off, r);
                         }
+                        tmem_wait_st();
                     }
-                    fence_proxy_async_smem();
+                    fence_before();
                     mbar_arrive(b_qfull);
                 }
                 const int j0 = si.a0 + cur.t * kTok;
@@ -483,7 +489,7 @@ int gcd_i(int x, int y) {
 template <int DQK, int DV>
 int smem_for(int stages) {
     using L = Layout<DQK, DV>;
-    return 1024 + L::kQBytes + stages * (L::kQc + L::kVc) * kChunkBytes + 2 * L::kPBytes + 256;
+    return 1024 + stages * (L::kQc + L::kVc) * kChunkBytes + 2 * L::kPBytes + 256;
 }
 
 template <typename T, int DQK, int DV>
