@@ -2,26 +2,37 @@
 """Benchmark of topk = 1 verify attention on GB300.
 
 One step = one verify_attn_paged call (work list -> split-KV prefix -> fused
-combine) over one synthetic batch resident in HBM. The default workload is the
-Llama-3.1-8B-shaped GQA verify batch (bf16, 32 q / 8 kv heads, head dim 128,
-bs 16, prefixes uniform in [1024, 8192], 4 drafts, page size 4, 2M-token
-pool). Prints one JSON line.
+combine) over one synthetic batch resident in HBM. The top-level line is the
+mixed serving batch (bf16, 64 q / 8 kv heads, qk 192 / v 128, bs 128,
+lognormal prefixes up to 65536, 2..5 drafts, page size 16, sliding window 4096
+on every other call); the other workloads of the suite -- long-context GQA,
+DeepSeek-V3-shaped absorbed MLA, Llama-3.1-8B-shaped GQA, the tiny fp32 case,
+the split-KV page's micro-benchmark shape at 4k / 16k / 64k, and the FP8,
+tree-verify and draft-extend batches -- follow, each with the same record,
+under "workloads". Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--suite LIST|none]
+                  [--impl ours|reference]
 
-Timing: W untimed calls, then K calls, each bracketed by CUDA events on the
-launching stream, with a 256 MiB write between calls (outside the events) so
-no call starts with a warm L2. The prefix kernel is timed on its own by events
-recorded inside the call (verify_attn_paged_profiled), which gives the live
-roofline figure. `e2e` repeats the measurement through host buffers: each step
-copies q and the per-call metadata from pinned host memory, runs the call and
-copies out / lse back, all inside the events. The KV cache is resident state
-(it is a cache) and is not copied.
+Timing (per workload): W untimed calls, then K calls, each bracketed by CUDA
+events on the launching stream, with a 256 MiB write between calls (outside
+the events) so no call starts with a warm L2. Call i uses the workload's
+window for call i. The prefix kernel is timed on its own by events recorded
+inside the call (verify_attn_paged_profiled), which gives the live roofline
+figure. `e2e` repeats the measurement through host buffers: each step copies q
+and the per-call metadata from pinned host memory, runs the call and copies
+out / lse back, all inside the events. The KV cache is resident state (it is
+a cache) and is not copied.
+
+The CPU leg, after the GPU timing, times the fp64 oracle on the host cores
+(all of them, and one) on a bounded sample of the call, and holds one GPU
+result per window against the oracle on sampled rows ("parity").
 
 Under torchrun (N > 1) every rank runs its own replica on its own batch (weak
 scaling, no collective on the data path); the time is the max over ranks.
---impl reference times the fp64 CPU oracle on bounded samples of the same
-workload (rank 0 only).
+Workloads on the absorbed-MLA kernel run on one GPU only. --impl reference
+times the fp64 CPU oracle on bounded samples of the same workload (rank 0
+only).
 """
 from __future__ import annotations
 
@@ -54,21 +65,76 @@ KERNEL_SOURCES = {  # files whose change invalidates a stored ncu traffic figure
 }
 
 
-def parse():
+HEADLINE = "mixed_serving"
+# the other workloads the default run measures (their figures go under "workloads")
+SUITE = ("long_context", "dsv3_mla", "llama8b_gqa", "tiny", "p3_4k", "p3_16k", "p3_64k",
+         "llama8b_fp8", "llama8b_tree", "draft_extend")
+
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="llama8b_gqa", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(synth.WORKLOADS),
+                    help="the workload of the top-level line")
+    ap.add_argument("--suite", default="default",
+                    help="comma-separated workloads measured after the top-level one and reported "
+                         "under 'workloads' ('default': %s; 'none': only the top-level one)"
+                         % ",".join(SUITE))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="CPU time budget of the oracle baseline sample")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
+                    help="CPU time budget of the oracle baseline sample on all host cores")
+    ap.add_argument("--cpu-seconds-1core", type=float, default=3.0,
+                    help="CPU time budget of the same oracle sample on one core")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU leg (oracle timing and the sampled parity check)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--compact-pool", action="store_true",
                     help="pool of 1.25x the pages the batch uses instead of the workload's own "
                          "pool size (same kernels and results; for profiler captures)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def suite_names(args) -> list[str]:
+    if args.suite == "none":
+        return []
+    names = list(SUITE) if args.suite == "default" else [x for x in args.suite.split(",") if x]
+    for n in names:
+        if n not in synth.WORKLOADS:
+            raise SystemExit(f"bench.py: unknown workload {n!r} in --suite")
+    return [n for n in names if n != args.workload]
+
+
+def plan_path(wl) -> int:
+    """The prefix path a workload's plan selects, decided on the host (the
+    plan reads no tensor and, given an SM count, touches no device)."""
+    from speculative_decoding_verify_topk_gb300 import binding
+    p, d = synth.draw_lengths(wl)
+    kv8 = wl.kv_dtype == torch.float8_e4m3fn
+    plan = binding.verify_attn_plan(
+        max_bs=wl.bs, max_draft=max(1, int(d.max())), num_q_heads=wl.num_q_heads,
+        num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim, v_dim=wl.v_dim, page_size=wl.page_size,
+        dtype=synth.DTYPE_CODES[wl.dtype], max_kv_len=max(1, int((p + d).max())), num_pages=1 << 20,
+        v_aliases_k=wl.v_aliases_k, num_sms=152, kv_dtype=binding.VA_FP8_E4M3 if kv8 else 0)
+    return int(plan.path)
+
+
+def single_gpu_only(name: str) -> bool:
+    """Workloads whose plan selects the absorbed-MLA kernel. That kernel loads
+    KV tiles with cluster-multicast bulk-tensor copies through a tensor map over
+    this GPU's own pool, a form kept to runs that use one GPU."""
+    from speculative_decoding_verify_topk_gb300 import binding
+    return plan_path(synth.WORKLOADS[name]) == binding.VA_PATH_MLA
+
+
+def multi_rank_refusal(args, world: int) -> str | None:
+    """Why a run under torchrun (world > 1) must not start, or None."""
+    if world > 1 and single_gpu_only(args.workload):
+        return (f"bench.py: workload {args.workload} runs the absorbed-MLA kernel, whose "
+                f"cluster-multicast loads are for single-GPU runs only; refusing to start "
+                f"{world} ranks (run it with --gpus 1, without torchrun)")
+    return None
 
 
 # ---------------------------------------------------------------------------
@@ -135,23 +201,33 @@ def kernel_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if its source digest matches the current sources."""
+def stored_profile(kernel: str, workload: str) -> dict:
+    """Figures from the committed ncu summary of this kernel on this workload
+    (profiles/<kernel>_<workload>.md): DRAM bytes per launch and, where given,
+    the tensor pipe's active share. Empty when there is no summary or its
+    source digest no longer matches the kernel's sources."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
-        return None
+        return {}
     fields = {}
     for line in open(path):
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_digest")):
-            k, v = line.strip().split(":", 1)
+        line = line.strip()
+        if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_digest",
+                                            "tensor_pipe_active_pct")):
+            k, v = line.split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("source_digest") != kernel_digest(kernel):
-        return None
+        return {}
+    out = {}
     try:
-        return int(float(fields["traffic_bytes_per_launch"]))
+        out["traffic"] = int(float(fields["traffic_bytes_per_launch"]))
     except (KeyError, ValueError):
-        return None
+        pass
+    try:
+        out["tensor_pipe_active_pct"] = float(fields["tensor_pipe_active_pct"])
+    except (KeyError, ValueError):
+        pass
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -215,11 +291,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle (baseline leg and reference arm)
+# CPU leg: the oracle timed on the host cores, and the sampled parity check
 # ---------------------------------------------------------------------------
 
-def oracle_rows_runner(pb_host: synth.Paged, window: int):
-    import oracle
+def oracle_kwargs(pb_host: synth.Paged, window: int):
+    """The oracle's arguments for a host copy of a batch (raw bits, CSR table)."""
     wl = pb_host.wl
     tree = synth.call_tree_masks(wl, pb_host.num_draft)
     args = (synth.raw_bits(pb_host.q), synth.raw_bits(pb_host.k_cache),
@@ -231,6 +307,15 @@ def oracle_rows_runner(pb_host: synth.Paged, window: int):
               scale=wl.scale, window=window, v_aliases_k=wl.v_aliases_k,
               kv_dtype=synth.DTYPE_CODES[wl.kv_type], k_scale=wl.k_scale, v_scale=wl.v_scale,
               tree_mask=None if tree is None else tree.numpy().astype(np.int64) & 0xFFFFFFFF)
+    return args, kw, tree
+
+
+def oracle_rows_runner(pb_host: synth.Paged, window: int, threads: int = 0):
+    """run(n): the oracle on the first n of the call's (b, i, h) rows in a
+    seeded random order; returns (seconds, the share of the call's key work)."""
+    import oracle
+    wl = pb_host.wl
+    args, kw, tree = oracle_kwargs(pb_host, window)
     p = pb_host.seq_lens.numpy().astype(np.int64)
     d = pb_host.num_draft.numpy().astype(np.int64)
     words = None if tree is None else (tree.numpy().astype(np.int64) & 0xFFFFFFFF).tolist()
@@ -246,7 +331,7 @@ def oracle_rows_runner(pb_host: synth.Paged, window: int):
             for h in range(wl.num_q_heads):
                 rows.append((b, i, h))
                 keys.append(k)
-    rows = np.array(rows, dtype=np.int32)
+    rows = np.array(rows, dtype=np.int32).reshape(-1, 3)
     keys = np.array(keys, dtype=np.float64)
     order = np.random.default_rng(12345).permutation(len(rows))
     rows, keys = rows[order], keys[order]
@@ -254,11 +339,11 @@ def oracle_rows_runner(pb_host: synth.Paged, window: int):
 
     def run(n):
         t0 = time.perf_counter()
-        oracle.verify_attn(*args, rows=rows[:n], **kw)
+        oracle.verify_attn(*args, rows=rows[:n], threads=threads, **kw)
         dt = time.perf_counter() - t0
         return dt, float(keys[:n].sum()) / total_keys
 
-    return run, len(rows), oracle.max_threads()
+    return run, len(rows), (oracle.max_threads() if threads == 0 else threads)
 
 
 def size_sample(run, n_rows, budget_s):
@@ -272,15 +357,53 @@ def size_sample(run, n_rows, budget_s):
     return max(1, min(n_rows, int(budget_s / max(per_row, 1e-9))))
 
 
-def cpu_baseline(pb_dev: synth.Paged, window: int, budget_s: float):
-    host = synth.subset(pb_dev, range(pb_dev.wl.bs))
-    run, n_rows, cores = oracle_rows_runner(host, window)
+def timed_oracle(host: synth.Paged, window: int, budget_s: float, threads: int = 0):
+    run, n_rows, cores = oracle_rows_runner(host, window, threads)
     n = size_sample(run, n_rows, budget_s)
     dt, frac = run(n)
-    calls_per_s = frac / dt
-    return {"value": calls_per_s, "unit": "calls/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {n_rows} query rows (random, seed 12345) of one call; "
-                      f"{frac * 100:.3f}% of the call's key work in {dt:.2f} s, scaled by key work"}
+    return {"value": frac / dt, "unit": "calls/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {n_rows} query rows (random, seed 12345) of one call with window "
+                      f"{window}; {frac * 100:.3f}% of the call's key work in {dt:.2f} s, scaled "
+                      f"by key work"}
+
+
+def sampled_parity(host: synth.Paged, window: int, out_dev, lse_dev) -> dict:
+    """The GPU's result of one call against the oracle on the rows
+    oracle.compare.sample_rows picks (the last draft row of every sequence, all
+    rows of the longest, the window's edge rows, and a random fill), held to
+    the parity bar."""
+    import oracle
+    from oracle import compare
+    wl = host.wl
+    rows = compare.sample_rows(host.seq_lens.numpy(), host.num_draft.numpy(), wl.num_q_heads,
+                               window, budget=2048, seed=wl.seed)
+    args, kw, _ = oracle_kwargs(host, window)
+    t0 = time.perf_counter()
+    ref_o, ref_l = oracle.verify_attn(*args, rows=rows, **kw)
+    dt = time.perf_counter() - t0
+    got_o, got_l = compare.gather_rows(out_dev.double().cpu().numpy(), lse_dev.double().cpu().numpy(),
+                                       rows, host.num_draft.numpy())
+    st = compare.error_stats(got_o, ref_o, got_l, ref_l)
+    atol, rtol, latol = compare.tolerance(wl.dtype == torch.float32)
+    bad = compare.failures(st, atol, rtol, latol)
+    st.update({"window": window, "pass": not bad, "bar": {"max_abs": atol, "max_rel": rtol,
+                                                          "lse_max_abs": latol},
+               "oracle_s": dt})
+    if bad:
+        st["failures"] = bad
+    return st
+
+
+def cpu_leg(pb_dev: synth.Paged, results: dict, budget_all: float, budget_one: float):
+    """Oracle on the host cores: calls/s on all cores and on one (bounded
+    samples of the call), plus the sampled parity of each window's GPU result
+    (results: window -> (out, lse) of one call)."""
+    host = synth.subset(pb_dev, range(pb_dev.wl.bs))
+    windows = list(results)
+    cpu = timed_oracle(host, windows[0], budget_all)
+    cpu["one_core"] = timed_oracle(host, windows[0], budget_one, threads=1)
+    parity = {str(w): sampled_parity(host, w, *results[w]) for w in windows}
+    return cpu, parity
 
 
 # ---------------------------------------------------------------------------
@@ -299,30 +422,37 @@ def reference_arm(args):
     if rank != 0:
         return
     wl = synth.WORKLOADS[args.workload]
-    window = wl.window_for_call(0)
     # same lengths, drafts and values; a compact pool (1.25x the pages used)
-    # instead of the device run's 2M-token pool, which changes no result
+    # instead of the device run's pool, which changes no result
     pb = synth.make_batch(wl.replace(pool_tokens=None), device="cpu")
-    run, n_rows, cores = oracle_rows_runner(pb, window)
+    windows = [wl.window_for_call(i) for i in range(len(wl.window))]
+    runners = {w: oracle_rows_runner(pb, w) for w in set(windows)}
     warmup = max(3, args.warmup)
     budget = max(0.02, min(3.0, 150.0 / (args.steps + warmup)))
-    n = size_sample(run, n_rows, budget)
-    for _ in range(warmup):
-        run(n)
-    times, frac = [], None
-    for _ in range(args.steps):
-        dt, frac = run(n)
+    sizes = {w: size_sample(r[0], r[1], budget) for w, r in runners.items()}
+    for i in range(warmup):
+        w = wl.window_for_call(i)
+        runners[w][0](sizes[w])
+    times, fracs = [], []
+    for i in range(args.steps):
+        w = wl.window_for_call(i)
+        dt, frac = runners[w][0](sizes[w])
         times.append(dt)
-    total = sum(times)
-    value = frac * args.steps / total
+        fracs.append(frac)
+    # each step is a sample of one call: scale its time by the key work it covered
+    call_s = [t / f for t, f in zip(times, fracs)]
+    total = sum(call_s)
+    value = args.steps / total
+    cores = runners[windows[0]][2]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "calls/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
-            "ms_per_step": 1000.0 * total / args.steps / frac, "higher_is_better": True,
+            "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "bs": wl.bs, "window": window},
+            "config": {"workload": wl.name, "bs": wl.bs, "windows": sorted(set(windows))},
             "cpu_baseline": {"value": value, "unit": "calls/s", "cores": cores, "kind": "oracle",
-                             "sample": f"each step: {n} of {n_rows} query rows of one call "
-                                       f"({frac * 100:.4f}% of its key work), scaled by key work"},
+                             "sample": "each step: " + ", ".join(
+                                 f"{sizes[w]} of {runners[w][1]} query rows (window {w})"
+                                 for w in sorted(sizes)) + " of one call, scaled by key work"},
             "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -352,80 +482,98 @@ def replica_seed(wl, rank: int) -> int:
     return wl.seed + 1000 * rank
 
 
-def ours_arm(args):
+def make_attention(pb: synth.Paged, device):
+    """The plan and workspace the bench times a batch with (the parity tests
+    at full size use the same)."""
     import speculative_decoding_verify_topk_gb300 as va
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
-    wl = synth.WORKLOADS[args.workload]
-    if args.compact_pool:
-        wl = wl.replace(pool_tokens=None)
-    window = wl.window_for_call(0)
-    pb = synth.make_batch(wl, device=dev, seed=replica_seed(wl, rank))
+    wl = pb.wl
     lens = pb.seq_lens.long() + pb.num_draft.long()
-    attn = va.VerifyAttention(max_bs=wl.bs, max_draft=int(pb.num_draft.max()),
+    return va.VerifyAttention(max_bs=wl.bs, max_draft=max(1, int(pb.num_draft.max())),
                               num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
                               qk_dim=wl.qk_dim, v_dim=wl.v_dim, page_size=pb.page_size,
-                              dtype=wl.dtype, max_kv_len=int(lens.max()), num_pages=pb.num_pages,
-                              v_aliases_k=wl.v_aliases_k, device=dev, kv_dtype=wl.kv_dtype)
+                              dtype=wl.dtype, max_kv_len=max(1, int(lens.max())),
+                              num_pages=pb.num_pages, v_aliases_k=wl.v_aliases_k, device=device,
+                              kv_dtype=wl.kv_dtype)
+
+
+class Caller:
+    """One workload's verify call with its outputs allocated once."""
+
+    def __init__(self, pb: synth.Paged, device, stream):
+        wl = pb.wl
+        self.pb, self.wl, self.stream = pb, wl, stream
+        self.attn = make_attention(pb, device)
+        self.out = torch.empty(pb.total_q, wl.num_q_heads, wl.v_dim, dtype=wl.dtype, device=device)
+        self.lse = torch.empty(pb.total_q, wl.num_q_heads, dtype=torch.float32, device=device)
+        self.vcache = None if wl.v_aliases_k else pb.v_cache
+        tree = synth.call_tree_masks(wl, pb.num_draft.cpu())
+        self.tree = None if tree is None else tree.to(device)
+
+    def __call__(self, window, events=None, q=None, pt=None, ip=None, sl=None, nd=None, tm=None,
+                 out=None, lse=None):
+        pb, wl = self.pb, self.wl
+        self.attn(pb.q if q is None else q, pb.k_cache, self.vcache,
+                  pb.page_table if pt is None else pt, pb.kv_indptr if ip is None else ip,
+                  pb.seq_lens if sl is None else sl, pb.num_draft if nd is None else nd,
+                  page_size=pb.page_size, scale=wl.scale, window=window,
+                  out=self.out if out is None else out, lse=self.lse if lse is None else lse,
+                  stream=self.stream, events=events, tree_mask=self.tree if tm is None else tm,
+                  k_scale=wl.k_scale, v_scale=wl.v_scale)
+
+
+def smi_target(dev) -> str:
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    return ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(dev.index)
+
+
+def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) -> dict | None:
+    """Times one workload (K calls after W warm-up ones, window of call i =
+    the workload's i-th) and returns its record (rank 0; None elsewhere)."""
+    import speculative_decoding_verify_topk_gb300 as va
     stream = torch.cuda.current_stream(dev)
-    out = torch.empty(pb.total_q, wl.num_q_heads, wl.v_dim, dtype=wl.dtype, device=dev)
-    lse = torch.empty(pb.total_q, wl.num_q_heads, dtype=torch.float32, device=dev)
-    vcache = None if wl.v_aliases_k else pb.v_cache
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    tree = synth.call_tree_masks(wl, pb.num_draft.cpu())
-    tree = None if tree is None else tree.to(dev)
-    acct = call_accounting(pb, window, tree)
+    pb = synth.make_batch(wl, device=dev, seed=replica_seed(wl, rank))
+    call = Caller(pb, dev, stream)
+    attn = call.attn
+    windows = [wl.window_for_call(i) for i in range(len(wl.window))]
+    accts = {w: call_accounting(pb, w, call.tree) for w in set(windows)}
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
+    win = lambda i: wl.window_for_call(i)
 
-    def call(events=None, q=pb.q, pt=pb.page_table, ip=pb.kv_indptr, sl=pb.seq_lens,
-             nd=pb.num_draft, o=out, l=lse, tm=tree):
-        attn(q, pb.k_cache, vcache, pt, ip, sl, nd, page_size=pb.page_size, scale=wl.scale,
-             window=window, out=o, lse=l, stream=stream, events=events, tree_mask=tm,
-             k_scale=wl.k_scale, v_scale=wl.v_scale)
-
-    for _ in range(warmup):
-        flush.zero_()
-        call()
-    torch.cuda.synchronize(dev)
-    if attn.check(stream) != 0:
-        raise RuntimeError("device range check failed during warm-up")
-
-    # ---- device-timed steps (L2 flushed between steps, outside the events)
-    ev_call = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-    prof_steps = min(steps, 500)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(prof_steps)]
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
+    for i in range(warmup):
+        flush.zero_()
+        call(win(i))
+    torch.cuda.synchronize(dev)
+    if attn.check(stream) != 0:
+        raise RuntimeError(f"{wl.name}: device range check failed during warm-up")
+
+    # ---- device-timed steps (L2 flushed between steps, outside the events)
+    ev_call = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
     barrier()
     torch.cuda.synchronize(dev)
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "") or "")
-    smi_target = ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(dev.index)
-    with ClockSampler(smi_target) as clk:
+    with ClockSampler(smi_target(dev)) as clk:
         for i in range(steps):
             flush.zero_()
             ev_call[i][0].record(stream)
-            call()
+            call(win(i))
             ev_call[i][1].record(stream)
         torch.cuda.synchronize(dev)
     barrier()
-    step_ms = [a_.elapsed_time(b_) for a_, b_ in ev_call]
-    total_ms = sum(step_ms)
-    # second pass, same steps: events recorded between the call's three kernels
+    total_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev_call)
+    # second pass: events recorded between the call's three kernels
     # (verify_attn_paged_profiled) time each kernel on its own stream
+    prof_steps = min(steps, 500)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(prof_steps)]
     for i in range(prof_steps):
         flush.zero_()
-        call(events=evs[i])
+        call(win(i), events=evs[i])
     torch.cuda.synchronize(dev)
     prefix_ms = [e[1].elapsed_time(e[2]) for e in evs]
     combine_ms = [e[2].elapsed_time(e[3]) for e in evs]
@@ -444,13 +592,13 @@ def ours_arm(args):
         d_q, d_pt, d_ip, d_sl, d_nd = (torch.empty_like(pb.q), torch.empty_like(pb.page_table),
                                        torch.empty_like(pb.kv_indptr), torch.empty_like(pb.seq_lens),
                                        torch.empty_like(pb.num_draft))
-        h_tm = None if tree is None else pin(tree)
-        d_tm = None if tree is None else torch.empty_like(tree)
-        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h_tm = None if call.tree is None else pin(call.tree)
+        d_tm = None if call.tree is None else torch.empty_like(call.tree)
+        h_out = torch.empty(call.out.shape, dtype=call.out.dtype, pin_memory=True)
+        h_lse = torch.empty(call.lse.shape, dtype=call.lse.dtype, pin_memory=True)
         e2e_steps = min(steps, 1000)
 
-        def e2e_step():
+        def e2e_step(i):
             d_q.copy_(h_q, non_blocking=True)
             d_pt.copy_(h_pt, non_blocking=True)
             d_ip.copy_(h_ip, non_blocking=True)
@@ -458,63 +606,83 @@ def ours_arm(args):
             d_nd.copy_(h_nd, non_blocking=True)
             if d_tm is not None:
                 d_tm.copy_(h_tm, non_blocking=True)
-            call(q=d_q, pt=d_pt, ip=d_ip, sl=d_sl, nd=d_nd, tm=d_tm)
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
+            call(win(i), q=d_q, pt=d_pt, ip=d_ip, sl=d_sl, nd=d_nd, tm=d_tm)
+            h_out.copy_(call.out, non_blocking=True)
+            h_lse.copy_(call.lse, non_blocking=True)
 
-        for _ in range(warmup):
+        for i in range(warmup):
             flush.zero_()
-            e2e_step()
+            e2e_step(i)
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(e2e_steps)]
         torch.cuda.synchronize(dev)
-        for a, b in ev2:
+        for i, (a, b) in enumerate(ev2):
             flush.zero_()
             a.record(stream)
-            e2e_step()
+            e2e_step(i)
             b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
-        if not torch.equal(h_out, out.cpu()):
-            raise RuntimeError("e2e result differs from the device result")
+        if not torch.equal(h_out, call.out.cpu()):
+            raise RuntimeError(f"{wl.name}: e2e result differs from the device result")
         h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_ip, h_sl, h_nd)
                   + (() if h_tm is None else (h_tm,)))
         d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
         e2e = {"value": job_rate(world, e2e_steps, e2e_ms), "unit": "calls/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / e2e_steps}
+               "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps}
 
-    builder = time_page_table_builder(pb, stream, dev, flush)
+    pt_builder = time_page_table_builder(pb, stream, dev, flush) if builder else None
+    # one result per window for the sampled parity check
+    results = {}
+    for w in sorted(set(windows), key=windows.index):
+        o = torch.empty_like(call.out)
+        l_ = torch.empty_like(call.lse)
+        call(w, out=o, lse=l_)
+        results[w] = (o, l_)
+    torch.cuda.synchronize(dev)
+    bits = attn.check(stream)
     if rank != 0:
-        return
+        return None
+
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    if builder is not None:
-        builder["frac_of_measured_hbm"] = builder["gbs"] / hbm_peak
+    if pt_builder is not None:
+        pt_builder["frac_of_measured_hbm"] = pt_builder["gbs"] / hbm_peak
     prefix_avg_ms = statistics.fmean(prefix_ms)
+    # algorithmic bytes / flops per step, averaged over the steps' windows
+    mean_of = lambda key, n: statistics.fmean(accts[win(i)][key] for i in range(n))
     kernel = {va.VA_PATH_MMA: "prefix_mma", va.VA_PATH_F32: "prefix_f32",
               va.VA_PATH_MLA: "prefix_mla", va.VA_PATH_TC: "prefix_tc"}[attn.plan.path]
-    traffic = stored_traffic(kernel, wl.name)
-    achieved = acct["prefix_bytes"] / (prefix_avg_ms * 1e-3) / 1e9
+    prof = stored_profile(kernel, wl.name)
+    prefix_bytes = sum(accts[win(i)]["prefix_bytes"] for i in range(prof_steps))
+    achieved = prefix_bytes / (sum(prefix_ms) * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic, "kernel": kernel,
-                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                "frac": achieved / hbm_peak, "traffic": prof.get("traffic"), "kernel": kernel,
+                "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": acct["prefix_bytes"],
+                "algorithmic_bytes_per_launch": mean_of("prefix_bytes", prof_steps),
                 "launch_ms": prefix_avg_ms}
     if attn.plan.path == va.VA_PATH_MLA:
-        tf = acct["flops"] / (prefix_avg_ms * 1e-3) / 1e12
-        roofline.update({"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]),
-                         "unit": "TFLOP/s", "frac": tf / float(peaks["bf16_tflops"]),
-                         "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json, burst)"
+        flops = sum(accts[win(i)]["flops"] for i in range(prof_steps))
+        tf = flops / (sum(prefix_ms) * 1e-3) / 1e12
+        burst, sustained = float(peaks["bf16_tflops"]), float(peaks.get("bf16_tflops_sustained", 0) or 0)
+        roofline.update({"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s",
+                         "frac": tf / burst,
+                         "peak_sustained": sustained or None,
+                         "frac_of_sustained": tf / sustained if sustained else None,
+                         "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json, burst)"
                          if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
-                         "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak})
-    cpu = None
+                         "algorithmic_flops_per_launch": mean_of("flops", prof_steps),
+                         "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak,
+                         "tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct")})
+    cpu = parity = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(pb, window, args.cpu_seconds)
-    kv_gbs = acct["kv_call"] / (ms_per_step * 1e-3) / 1e9
-    line = {
+        cpu, parity = cpu_leg(pb, results, args.cpu_seconds, args.cpu_seconds_1core)
+    kv_call = mean_of("kv_call", steps)
+    kv_gbs = kv_call / (ms_per_step * 1e-3) / 1e9
+    rec = {
         "metric": METRIC, "value": value, "unit": "calls/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
@@ -523,27 +691,68 @@ def ours_arm(args):
         "data": "synthetic (seeded N(0,1) Q/K/V, NaN-poisoned unowned pool slots)",
         "config": {"workload": wl.name, "bs": wl.bs, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "qk_dim": wl.qk_dim, "v_dim": wl.v_dim,
-                   "page_size": pb.page_size, "num_pages": pb.num_pages, "window": window,
+                   "page_size": pb.page_size, "num_pages": pb.num_pages,
+                   "windows": [win(i) for i in range(len(wl.window))],
                    "prefix": list(wl.prefix), "draft": list(wl.draft),
-                   "kv_tokens": int(lens.sum()), "num_ctas": attn.plan.num_ctas,
-                   "tree": wl.tree,
+                   "kv_tokens": int((pb.seq_lens.long() + pb.num_draft.long()).sum()),
+                   "num_ctas": attn.plan.num_ctas, "tree": wl.tree,
                    "kv_dtype": str(wl.kv_type).replace("torch.", ""),
                    "l2": "flushed between steps (256 MiB write outside the timed events)"},
         "kv_gbs": kv_gbs,
         "kv_frac_of_measured_hbm": kv_gbs / hbm_peak,
         "kv_frac_of_8tbs": kv_gbs / 8000.0,
-        "call_gbs": acct["call_bytes"] / (ms_per_step * 1e-3) / 1e9,
+        "call_gbs": mean_of("call_bytes", steps) / (ms_per_step * 1e-3) / 1e9,
         "stage_ms": {"worklist": statistics.fmean(worklist_ms), "prefix": prefix_avg_ms,
                      "combine": statistics.fmean(combine_ms),
                      "call_with_stage_events": statistics.fmean(profiled_step_ms),
                      "steps": prof_steps},
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": e2e,
-        "page_table_builder": builder,
         "gpu_launches": attn.launches_per_call * steps,
+        "device_error_bits": bits,
         "clocks": clk.summary(),
     }
+    if pt_builder is not None:
+        rec["page_table_builder"] = pt_builder
+    return rec
+
+
+def ours_arm(args):
+    world, rank, local = dist_env()
+    refusal = multi_rank_refusal(args, world)
+    if refusal:
+        print(refusal, file=sys.stderr, flush=True)
+        raise SystemExit(2)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    names = suite_names(args)
+    skipped = {}
+    if world > 1:
+        for n in [n for n in names if single_gpu_only(n)]:
+            names.remove(n)
+            skipped[n] = "single-GPU runs only (cluster-multicast loads)"
+
+    def wl_of(name):
+        wl = synth.WORKLOADS[name]
+        return wl.replace(pool_tokens=None) if args.compact_pool else wl
+
+    line = measure(wl_of(args.workload), args, dev, world, rank, flush, builder=True)
+    torch.cuda.empty_cache()
+    subs = {}
+    for name in names:
+        subs[name] = measure(wl_of(name), args, dev, world, rank, flush)
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return
+    if names or skipped:
+        line["workloads"] = {**subs, **{n: {"skipped": why} for n, why in skipped.items()}}
     print(json.dumps(line), flush=True)
 
 

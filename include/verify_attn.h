@@ -280,6 +280,11 @@ int verify_attn_launches_per_call(const va_plan *plan);
  *   call left; the kernels need none of it to start cleared. Calls whose
  *   executions overlap on the GPU (different streams, or different host
  *   threads) race on the array: order them on one stream.
+ * - The device address is looked up once per device and kept for the life of
+ *   the process: a program that resets a device (cudaDeviceReset) after its
+ *   first call there must not call this entry point on that device again.
+ * Device-side range errors set the array's error word, as with a caller
+ * workspace; verify_attn_check_static reads it.
  * Returns the codes of verify_attn_paged.
  */
 #define VA_STATIC_WORKSPACE_BYTES (32u << 20)
@@ -288,6 +293,15 @@ int verify_attn_paged_static(const va_plan *plan, int bs, const void *q, const v
                              const int32_t *kv_indptr, const int32_t *seq_lens,
                              const int32_t *num_draft, int page_size, float scale, int window,
                              void *out, float *lse, void *stream);
+
+/*
+ * verify_attn_check for verify_attn_paged_static, whose workspace the caller
+ * never sees: synchronises the stream, reads the error word that the last
+ * static call on the current device left, and stores it in *error_bits (if not
+ * NULL). Returns VA_OK, VA_DEVICE_RANGE_ERROR when any bit is set, or
+ * VA_CUDA_ERROR. Allocates nothing.
+ */
+int verify_attn_check_static(void *stream, int32_t *error_bits);
 
 /*
  * Builds the page-level table verify_attn_paged reads from token-level KV

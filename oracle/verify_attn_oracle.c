@@ -432,13 +432,15 @@ int oracle_verify_attn(int bs, int hq, int hkv, int dqk, int dv, int page_size, 
         }
     }
 
+    /* the thread count of this call only (a num_threads clause, so a
+     * one-thread call leaves later calls on the default count) */
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
+    const int nthreads = threads > 0 ? threads : omp_get_max_threads();
 #else
     (void)threads;
 #endif
 
-#pragma omp parallel
+#pragma omp parallel num_threads(nthreads)
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)max_keys);
         int local = (s == NULL) ? ORACLE_NO_MEMORY : ORACLE_OK;

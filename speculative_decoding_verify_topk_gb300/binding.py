@@ -21,7 +21,8 @@ VA_ERR_BAD_PAGE, VA_ERR_SHORT_TABLE, VA_ERR_BAD_DRAFT, VA_ERR_BAD_LENGTH, VA_ERR
 EXPORTS = ("verify_attn_plan", "verify_attn_paged", "verify_attn_paged_profiled",
            "verify_attn_status_string", "verify_attn_check", "verify_attn_launches_per_call",
            "verify_attn_paged_static", "verify_attn_last_error", "verify_attn_build_page_table",
-           "verify_attn_paged_tree", "verify_attn_paged_scaled", "verify_attn_selftest_timeout")
+           "verify_attn_paged_tree", "verify_attn_paged_scaled", "verify_attn_selftest_timeout",
+           "verify_attn_check_static")
 
 
 class Problem(ctypes.Structure):

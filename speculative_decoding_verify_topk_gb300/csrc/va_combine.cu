@@ -202,8 +202,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    store_row<T, VPL>(og, acc, 1.f / z);
-    if (lane == 0) a.lse[qrow] = (mx + __log2f(z)) * 0.69314718055994531f;
+    // z == 0: the row sees no key at all (tree verify over an empty prefix with
+    // no draft bit set); its output is zeros and its lse -inf
+    store_row<T, VPL>(og, acc, z > 0.f ? 1.f / z : 0.f);
+    if (lane == 0) a.lse[qrow] = z > 0.f ? (mx + __log2f(z)) * 0.69314718055994531f : -INFINITY;
 }
 
 template <typename T, int VPL>

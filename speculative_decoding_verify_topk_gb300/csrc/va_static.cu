@@ -64,3 +64,20 @@ extern "C" int verify_attn_paged_static(const va_plan* plan, int bs, const void*
     return va::run(plan, bs, q, k_cache, v_cache, page_table, kv_indptr, seq_lens, num_draft,
                    page_size, scale, window, out, lse, ws, stream, nullptr);
 }
+
+extern "C" int verify_attn_check_static(void* stream, int32_t* error_bits) {
+    void* ws = nullptr;
+    const int st = static_workspace(&ws);
+    if (st != VA_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return VA_CUDA_ERROR;
+    }
+    int32_t word = 0;   // header word 0 of the workspace: the device error bits
+    if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return VA_CUDA_ERROR;
+    }
+    if (error_bits) *error_bits = word;
+    return word ? VA_DEVICE_RANGE_ERROR : VA_OK;
+}

@@ -24,6 +24,9 @@ Workloads (all Q/K/V drawn from N(0, 1) in fp32, then cast):
                   lognormal (median 2048, sigma 1) clipped to [1, 65536], 2..5
                   drafts per sequence, page size 16, sliding window 4096 on
                   every other call
+  p3_4k, p3_16k,  the split-KV page's micro-benchmark shape: bf16, bs 1, 16 / 2
+  p3_64k          heads, head dim 256, 4 drafts, prefix 4096 / 16384 / 65536,
+                  page size 16
 
 Where a pool size is not given it holds 1.25x the pages the batch needs. Pool
 slots that no sequence owns, and the tail of each sequence's last page, hold
@@ -95,6 +98,13 @@ WORKLOADS = {
     "draft_extend": Workload("draft_extend", torch.bfloat16, 64, 32, 8, 128, 128, 16,
                              ("uniform", 1024, 8192), ("choice", [1, 2, 3, 4, 5]), 5,
                              1.0 / math.sqrt(128)),
+    # the micro-benchmark shape of "Split-KV flash-decode attention for EAGLE
+    # target-verify (Triton backend)", Speed Tests and Profiling: one sequence,
+    # 16 q-heads / 2 kv-heads, head dim 256, 4 drafts, at three context lengths
+    # (the page size is not stated there; 16 is this build's reading)
+    **{f"p3_{n // 1024}k": Workload(f"p3_{n // 1024}k", torch.bfloat16, 1, 16, 2, 256, 256, 16,
+                                    ("fixed", [n]), ("fixed", 4), 5, 1.0 / math.sqrt(256))
+       for n in (4096, 16384, 65536)},
     # the Llama-3.1-8B-shaped batch over an FP8 E4M3 KV cache with per-tensor
     # scales (K / k_scale and V / v_scale stored)
     "llama8b_fp8": Workload("llama8b_fp8", torch.bfloat16, 16, 32, 8, 128, 128, 4,

@@ -57,3 +57,40 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.job_rate(1, 10, 1000.0) == 10.0
+
+
+def _torchrun(args, timeout=300):
+    import subprocess
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(ROOT, "bench.py")] + args
+    env = {**os.environ, "PYTHONPATH": ROOT}
+    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=timeout)
+
+
+@pytest.fixture(scope="module")
+def built_library():
+    sys.path.insert(0, ROOT)
+    from speculative_decoding_verify_topk_gb300 import build
+    build.build()
+
+
+def test_multi_rank_run_refuses_the_mla_workload(built_library):
+    """Two ranks of `bench.py --workload dsv3_mla` (the absorbed-MLA kernel,
+    whose cluster-multicast loads are kept to single-GPU runs) stop with a
+    nonzero status and say why, before either rank touches a GPU."""
+    res = _torchrun(["--gpus", "2", "--workload", "dsv3_mla", "--steps", "2", "--warmup", "3"])
+    assert res.returncode != 0
+    assert "single-GPU runs only" in res.stdout + res.stderr
+
+
+def test_refusal_covers_only_the_mla_path(built_library):
+    sys.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_verify_topk_gb300 import synth
+    mla = [n for n in synth.WORKLOADS if bench.single_gpu_only(n)]
+    assert mla == ["dsv3_mla"]
+    args = bench.parse(["--workload", "dsv3_mla"])
+    assert bench.multi_rank_refusal(args, 1) is None          # one GPU: allowed
+    assert "single-GPU" in bench.multi_rank_refusal(args, 2)
+    assert bench.multi_rank_refusal(bench.parse([]), 2) is None   # the default line is GQA

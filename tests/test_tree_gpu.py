@@ -109,3 +109,25 @@ def test_tree_rejects_window_and_missing_mask():
         va.verify_attn_paged_tree(attn.plan, wl.bs, pb.q, pb.k_cache, pb.v_cache, pb.page_table,
                                   pb.kv_indptr, pb.seq_lens, pb.num_draft, None, pb.page_size, wl.scale,
                                   out, lse, attn.workspace)
+
+
+@pytest.mark.parametrize("name", ["llama8b_gqa", "mixed_serving", "dsv3_mla", "tiny"])
+def test_tree_row_that_sees_no_key(name):
+    """An empty prefix and a row whose mask word is 0: the row sees no key at
+    all and gets zeros with lse = -inf, on every prefix path, next to rows and
+    sequences that see keys."""
+    wl = small(name, bs=3)
+    d_max = 4 if name == "tiny" else (6 if name == "dsv3_mla" else 8)
+    lg = synth.make_logical(wl, seq_lens=[0, 70, 0], num_draft=[3, 2, d_max])
+    pb = synth.paginate(lg) if name != "tiny" else synth.paginate(lg, pool_pages=512)
+    words = synth.tree_masks(synth.draft_trees(pb.num_draft.tolist(), seed=6)).clone()
+    words[0] = 0                     # sequence 0, row 0: no prefix and no draft bit
+    words[5] = 0                     # sequence 2, row 0: likewise
+    got_o, got_l = run_tree(pb, words)
+    ref_o, ref_l = oracle_on(pb, tree_mask=words.numpy())
+    assert np.isneginf(ref_l[0]).all() and np.isneginf(ref_l[5]).all()
+    assert (got_o[0] == 0).all() and (got_o[5] == 0).all()
+    assert np.isneginf(got_l[0]).all() and np.isneginf(got_l[5]).all()
+    atol, rtol, latol = tolerance(pb.wl.dtype)
+    assert_close("tree out", got_o, ref_o, atol, rtol)
+    assert_close("tree lse", got_l, ref_l, latol, 0.0)

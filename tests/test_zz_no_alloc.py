@@ -3,20 +3,23 @@ device memory (for example a plugin inside a host program that owns all device
 memory, or a latency-critical path where cudaMalloc is not allowed). Its
 scratch is a static device array inside the library.
 
-Checked through the C ABI against verify_attn_paged with a caller-provided
-workspace, on two calls in a row with different batches, so that whatever the
-first call leaves in the shared static array cannot leak into the second."""
+Checked through the C ABI against the fp64 oracle and against
+verify_attn_paged with a caller-provided workspace, on two calls in a row with
+different batches (each planned for its own pool), so that whatever the first
+call leaves in the shared static array cannot leak into the second. The
+device error word of the static array is read back with
+verify_attn_check_static: clean after good calls, flagged after a page id
+outside the pool."""
 from __future__ import annotations
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import speculative_decoding_verify_topk_gb300 as va
 from speculative_decoding_verify_topk_gb300 import binding, synth
-from va_helpers import assert_close, tolerance
+from va_helpers import assert_close, oracle_on, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -32,13 +35,23 @@ def lib():
     lib.verify_attn_paged_static.argtypes = [ctypes.POINTER(binding.Plan), I, P, P, P, P, P, P, P,
                                              I, ctypes.c_float, I, P, P, P]
     lib.verify_attn_paged_static.restype = I
+    lib.verify_attn_check_static.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+    lib.verify_attn_check_static.restype = I
     return lib
 
 
 def _batch(seed, bs):
     wl = synth.WORKLOADS["mixed_serving"].replace(bs=bs, prefix=("lognormal", 300.0, 1.0, 1, 3000),
                                                   pool_tokens=None)
-    return synth.make_batch(wl, seed=seed).to("cuda")
+    return synth.make_batch(wl, seed=seed)
+
+
+def _attention(pb):
+    wl = pb.wl
+    return va.VerifyAttention(max_bs=wl.bs, max_draft=5, num_q_heads=wl.num_q_heads,
+                              num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim, v_dim=wl.v_dim,
+                              page_size=pb.page_size, dtype=wl.dtype, max_kv_len=1 << 16,
+                              num_pages=pb.num_pages)
 
 
 def _static_call(lib, plan, pb, window):
@@ -57,27 +70,47 @@ def _static_call(lib, plan, pb, window):
     return out, lse
 
 
-def test_static_workspace_matches_caller_workspace(lib):
+def _static_bits(lib):
+    bits = ctypes.c_int32(-1)
+    rc = lib.verify_attn_check_static(torch.cuda.current_stream().cuda_stream, ctypes.byref(bits))
+    assert rc in (binding.VA_OK, binding.VA_DEVICE_RANGE_ERROR), binding.status_string(rc)
+    assert (rc == binding.VA_OK) == (bits.value == 0)
+    return bits.value
+
+
+def test_static_workspace_matches_oracle_and_caller_workspace(lib):
     torch.cuda.set_device(0)
-    first, second = _batch(31, 12), _batch(32, 7)
-    wl = first.wl
-    pool_pages = max(first.num_pages, second.num_pages)
-    attn = va.VerifyAttention(max_bs=12, max_draft=5, num_q_heads=wl.num_q_heads,
-                              num_kv_heads=wl.num_kv_heads, qk_dim=wl.qk_dim, v_dim=wl.v_dim,
-                              page_size=first.page_size, dtype=wl.dtype, max_kv_len=1 << 16,
-                              num_pages=pool_pages)
-    assert attn.plan.workspace_bytes <= STATIC_BYTES
-    atol, rtol, latol = tolerance(wl.dtype)
-    for pb, window in ((first, -1), (second, 200)):
-        plan = attn.plan
-        plan.problem.num_pages = pb.num_pages      # page ids are checked against this pool
-        ref_o, ref_l = attn(pb.q, pb.k_cache, pb.v_cache, pb.page_table, pb.kv_indptr,
-                            pb.seq_lens, pb.num_draft, page_size=pb.page_size, scale=wl.scale,
-                            window=window)
+    for seed, bs, window in ((31, 12, -1), (32, 7, 200)):
+        host = _batch(seed, bs)
+        pb = host.to("cuda")
+        wl = pb.wl
+        attn = _attention(pb)
+        assert attn.plan.workspace_bytes <= STATIC_BYTES
+        atol, rtol, latol = tolerance(wl.dtype)
+        got_o, got_l = _static_call(lib, attn.plan, pb, window)
+        assert _static_bits(lib) == 0
+        ref_o, ref_l = oracle_on(host, window=window)
+        assert_close("static out", got_o.double().cpu().numpy(), ref_o, atol, rtol)
+        assert_close("static lse", got_l.double().cpu().numpy(), ref_l, latol, 0)
+        ws_o, ws_l = attn(pb.q, pb.k_cache, pb.v_cache, pb.page_table, pb.kv_indptr, pb.seq_lens,
+                          pb.num_draft, page_size=pb.page_size, scale=wl.scale, window=window)
         assert attn.check() == 0
-        got_o, got_l = _static_call(lib, plan, pb, window)
-        assert_close("out", got_o.double().cpu().numpy(), ref_o.double().cpu().numpy(), atol, rtol)
-        assert_close("lse", got_l.double().cpu().numpy(), ref_l.double().cpu().numpy(), latol, 0)
+        # the same kernels on the same plan: the same bits
+        assert torch.equal(got_o, ws_o) and torch.equal(got_l, ws_l)
+
+
+def test_static_error_word_reports_bad_pages(lib):
+    torch.cuda.set_device(0)
+    host = _batch(33, 5)
+    pb = host.to("cuda")
+    attn = _attention(pb)
+    bad = synth.Paged(**{**pb.__dict__})
+    bad.page_table = pb.page_table.clone()
+    bad.page_table[int(pb.kv_indptr[2])] = pb.num_pages + 9    # sequence 2: outside the pool
+    _static_call(lib, attn.plan, bad, -1)
+    assert _static_bits(lib) & binding.VA_ERR_BAD_PAGE
+    _static_call(lib, attn.plan, pb, -1)                       # the next clean call clears it
+    assert _static_bits(lib) == 0
 
 
 def test_static_rejects_plans_beyond_its_size(lib):

@@ -7,6 +7,7 @@ import torch
 from scipy.special import logsumexp
 
 import oracle
+from oracle import compare
 from speculative_decoding_verify_topk_gb300 import synth
 
 
@@ -74,21 +75,31 @@ def brute_force(lg: synth.Logical, window: int = -1, scale=None, tree_parents=No
 
 def tolerance(dtype: torch.dtype):
     """(atol, rtol, lse_atol): bf16/fp16 inputs with fp32 accumulation are held to
-    1e-2 / 1e-2 on outputs and 1e-3 on the log-sum-exp, fp32 inputs to 1e-4."""
-    if dtype == torch.float32:
-        return 1e-4, 1e-4, 1e-4
-    return 1e-2, 1e-2, 1e-3
+    max abs 1e-2 and max relative 1e-2 on outputs and 1e-3 absolute on the
+    log-sum-exp; fp32 inputs to 1e-4 on all three (oracle/compare.py states
+    how each is measured)."""
+    return compare.tolerance(dtype == torch.float32)
 
 
 def assert_close(name, got, ref, atol, rtol):
+    """rtol > 0: an output array [..., v_dim], held separately to max abs error
+    <= atol and max relative error (per output vector, max norm) <= rtol.
+    rtol == 0: a log-sum-exp array, held to max abs error <= atol (a row that
+    sees no key has lse = -inf on both sides)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
-    assert np.isfinite(got).all(), f"{name}: non-finite values ({np.count_nonzero(~np.isfinite(got))})"
-    err = np.abs(got - ref)
-    bad = err > atol + rtol * np.abs(ref)
-    if bad.any():
-        idx = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(ref))), err.shape)
-        raise AssertionError(
-            f"{name}: {int(bad.sum())} of {bad.size} elements outside |d| <= {atol} + {rtol}|ref|;"
-            f" worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}; max abs err {err.max():.3e}")
+    if rtol > 0:
+        st = compare.error_stats(got, ref)
+        bad = compare.failures(st, atol, rtol, np.inf)
+    else:
+        st = compare.error_stats(np.zeros((got.size, 1)), np.zeros((got.size, 1)), got, ref)
+        bad = [] if st["lse_max_abs"] <= atol else [f"max abs error {st['lse_max_abs']:.3e} > {atol}"]
+    if bad:
+        err = np.abs(got - ref)
+        err[~np.isfinite(got)] = np.inf
+        if rtol == 0:
+            err[np.isneginf(got) & np.isneginf(ref)] = 0.0
+        idx = np.unravel_index(np.argmax(err), err.shape)
+        raise AssertionError(f"{name}: {'; '.join(bad)}; worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}"
+                             f" ({st})")
