@@ -167,10 +167,11 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         ctas_per_sm = 1;
     } else {
         // bf16 / fp16: a CTA takes hg kv-heads (the largest divisor of Hkv with
-        // hg * mt <= 8 consumer warps) over 16-token tiles fed by TMA boxes of
+        // hg * mt <= 8 consumer warps, 4 at v_dim 256) over 16-token tiles fed by TMA boxes of
         // gcd(page_size, 16) tokens
         const int mt = (out.rows_cap + 15) / 16;
-        if (mt > 8 || !va::prefix_mma_built(p.qk_dim, p.v_dim, kv8)) return VA_UNSUPPORTED;
+        const int max_nc = va::mma_max_consumers(p.v_dim);
+        if (mt > max_nc || !va::prefix_mma_built(p.qk_dim, p.v_dim, kv8)) return VA_UNSUPPORTED;
         // the most kv-heads per CTA (a divisor of Hkv, hg * mt <= 8 warps) that
         // still leaves room for a ring of at least three stages (two at worst)
         const int tb = va::gcd_int(p.page_size, 16);
@@ -178,12 +179,13 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         int hg = 0, box_stride = 0, stage = 0, stages = 0;
         for (int want = 3; want >= 2 && hg == 0; --want) {
             for (int d = 8; d >= 1; --d) {
-                if (p.num_kv_heads % d != 0 || d * mt > 8) continue;
+                if (p.num_kv_heads % d != 0 || d * mt > max_nc) continue;
                 const int bstr = (tb * d * 128 + 1023) / 1024 * 1024;
                 const int stg = (p.qk_dim / slice + p.v_dim / slice) * (16 / tb) * bstr;
                 // FP8: each consumer warp's fp16 copy of its head's tile (16 tokens)
                 const int staging = kv8 ? d * mt * (p.qk_dim / 64 + p.v_dim / 64) * 2048 : 0;
-                const int n = (kSmemLimit - 2048 - staging) / stg;
+                const int qsm = d * mt * va::mma_query_smem_per_warp(p.qk_dim);
+                const int n = (kSmemLimit - 2048 - staging - qsm) / stg;
                 if (n >= want) {
                     hg = d; box_stride = bstr; stage = stg; stages = n > 8 ? 8 : n;
                     break;
@@ -356,7 +358,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         const va::MmaLaunch fn = va::mma_launcher(p.qk_dim, p.v_dim, kv8);
         const int64_t slots = p.num_pages * p.page_size;
         CUtensorMap kmap, vmap;
-        if (!fn || g.nc < 1 || g.nc > 8 || g.ppt * g.tb != plan->tile_tokens ||
+        if (!fn || g.nc < 1 || g.nc > va::mma_max_consumers(p.v_dim) || g.ppt * g.tb != plan->tile_tokens ||
             g.stage_bytes != (g.nhk + g.nhv) * g.half_bytes)
             return VA_INVALID_ARG;
         const int pool_dtype = kv8 ? VA_FP8_E4M3 : p.dtype;

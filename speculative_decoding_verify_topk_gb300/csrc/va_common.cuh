@@ -126,6 +126,20 @@ struct Geo {
     uint32_t tx_box;       // bytes one box delivers
 };
 
+// Warp-level GQA kernel: bytes of shared memory each consumer warp keeps its
+// 16 query rows in. Above qk_dim 192 the query no longer fits in registers
+// beside a v_dim-wide accumulator (a warp's A fragments of 16 x 256 values are
+// 64 registers), so it is read from shared memory per k-step instead.
+__host__ __device__ constexpr int mma_query_smem_per_warp(int qk_dim) {
+    return qk_dim >= 256 ? 16 * qk_dim * 2 : 0;
+}
+
+// Warp-level GQA kernel: most consumer warps (kv-heads x 16-row tiles) a CTA
+// runs. A v_dim of 256 keeps 128 accumulator registers per thread, more than
+// the 168 a 9-warp block may hold, so those kernels run at most 4 consumers
+// (5 warps, up to 255 registers each).
+__host__ __device__ constexpr int mma_max_consumers(int v_dim) { return v_dim >= 256 ? 4 : 8; }
+
 // Host-side launchers (one per translation unit).
 cudaError_t launch_worklist(const Args& a, cudaStream_t s);
 cudaError_t launch_prefix_f32(const Args& a, cudaStream_t s);

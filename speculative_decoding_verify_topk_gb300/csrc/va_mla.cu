@@ -410,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < kTok; ++j) {   // -inf (an invisible key) gives exactly 0
-                    const float x = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -mu));
+                    // rounded to bf16 here, so the row sum is that of the weights
+                    // P V multiplies (the output stays a weighted mean)
+                    const float x = __bfloat162float(__float2bfloat16_rn(ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -mu))));
                     ps4[j & 3] += x;
                     r[j] = __float_as_uint(x);
                 }

@@ -74,6 +74,9 @@ struct Mma<__nv_bfloat16> {
         __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
+    static __device__ __forceinline__ float round(float x) {
+        return __bfloat162float(__float2bfloat16_rn(x));
+    }
 };
 
 template <>
@@ -90,6 +93,7 @@ struct Mma<__half> {
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
+    static __device__ __forceinline__ float round(float x) { return __half2float(__float2half_rn(x)); }
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2,
@@ -142,21 +146,25 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t x) {
 }
 
 constexpr int kTT = 16;            // tokens per tile
-constexpr int kMaxConsumers = 8;   // consumer warps per CTA (HG * MT)
-constexpr int kThreads = (kMaxConsumers + 1) * 32;
+// threads of a block: up to mma_max_consumers(DV) consumer warps and the producer
+__host__ __device__ constexpr int block_threads(int dv) { return (mma_max_consumers(dv) + 1) * 32; }
 
 template <typename T, int DQK, int DV, bool KV8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads(DV), 1)
     prefix_mma_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, Args a, Geo geo) {
     // tensor-core operand type: the query's, or fp16 over an FP8 cache
     using MT = typename std::conditional<KV8, __half, T>::type;
+    // QS: the query's A fragments come from shared memory (ldmatrix per k-step)
+    constexpr int kQSmem = mma_query_smem_per_warp(DQK);
+    constexpr bool QS = kQSmem > 0;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB alignment for the 128-byte swizzle atoms
     unsigned char* const ring =
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* const staging = ring + geo.stages * geo.stage_bytes;   // KV8: nc areas
-    unsigned char* const bars = staging + geo.nc * geo.staging_bytes;
+    unsigned char* const qsmem = staging + geo.nc * geo.staging_bytes;    // QS: nc areas
+    unsigned char* const bars = qsmem + geo.nc * kQSmem;
     const uint32_t bar_full = smem_u32(bars);                 // [stages], count 1 (+ tx)
     const uint32_t bar_empty = bar_full + 8 * geo.stages;     // [stages], count nc
     __shared__ int abort_flag;
@@ -281,7 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // =================== consumer warps ===================
         const int gl = warp / geo.mt, wm = warp - gl * geo.mt;   // head in group, m16 tile
         const int mi = lane >> 3, r8 = lane & 7;
-        uint32_t qf[DQK / 16][4];
+        uint32_t qf[QS ? 1 : DQK / 16][4];
+        // QS: this warp's 16 query rows, [row][DQK * 2 bytes], the 16-byte chunks
+        // of each 128-byte group XOR-swizzled by the row (conflict-free ldmatrix)
+        unsigned char* const qw = qsmem + warp * kQSmem;
+        auto qchunk = [](int row, int c) -> uint32_t {
+            return (uint32_t)(row * (DQK * 2) + (((c & ~7) | ((c & 7) ^ (row & 7))) << 4));
+        };
         float o[DV / 8][4];
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         int rows_b = 0, lo_r[2] = {0, 0}, hi_r[2] = {0, 0};
@@ -310,10 +324,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (seg_begin) {
                 si = a.seq[cur.b];
                 rows_b = a.group * si.draft;
+                if constexpr (QS) {
+                    // the warp's 16 rows into its query area (zeros past rows_b)
+                    __syncwarp();   // the previous segment's ldmatrix reads are done
+                    constexpr int kChunks = DQK / 8;   // 16-byte chunks per row
+#pragma unroll 4
+                    for (int it = lane; it < 16 * kChunks; it += 32) {
+                        const int rr = it / kChunks, c = it - rr * kChunks;
+                        const int r = wm * 16 + rr;
+                        uint4 x = make_uint4(0, 0, 0, 0);
+                        if (r < rows_b) {
+                            const int i = r / a.group, hh = r - i * a.group;
+                            x = __ldg(reinterpret_cast<const uint4*>(
+                                qg + ((int64_t)(si.qoff + i) * a.hq + g * a.group + hh) * DQK) + c);
+                            x = make_uint4(to_mma_pair<T, KV8>(x.x), to_mma_pair<T, KV8>(x.y),
+                                           to_mma_pair<T, KV8>(x.z), to_mma_pair<T, KV8>(x.w));
+                        }
+                        *reinterpret_cast<uint4*>(qw + qchunk(rr, c)) = x;
+                    }
+                    __syncwarp();
+                }
                 // query A fragments of rows wm*16 + lane/4 (+ 8), straight from global
                 const int c2 = 2 * (lane & 3);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < 2 && !QS; ++h) {
                     const int r = wm * 16 + (lane >> 2) + 8 * h;
                     const T* qrow = qg;
                     const bool live = r < rows_b;
@@ -423,8 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + (kk >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
                 float (&acc)[2][4] = (kk & 1) ? s2 : s;
-                Mma<MT>::run(acc[0], qf[kk], b0, b1);
-                Mma<MT>::run(acc[1], qf[kk], b2, b3);
+                if constexpr (QS) {
+                    // A fragments: lane l addresses row (l & 7) + 8 ((l >> 3) & 1) of the
+                    // 16, 8-column chunk 2 kk + (l >> 4)
+                    uint32_t qa[4];
+                    ldsm_x4(smem_u32(qw) + qchunk(r8 + 8 * (mi & 1), 2 * kk + (mi >> 1)), qa[0], qa[1],
+                            qa[2], qa[3]);
+                    Mma<MT>::run(acc[0], qa, b0, b1);
+                    Mma<MT>::run(acc[1], qa, b2, b3);
+                } else {
+                    Mma<MT>::run(acc[0], qf[kk], b0, b1);
+                    Mma<MT>::run(acc[1], qf[kk], b2, b3);
+                }
             }
 #pragma unroll
             for (int n = 0; n < 2; ++n)
@@ -473,7 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < 2; ++n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p = ex2_approx(s[n][e] - m_use[e >> 1]);
+                    // rounded to the operand type here, so the row sum is that of
+                    // the weights P V multiplies (the output stays a weighted mean)
+                    const float p = Mma<MT>::round(ex2_approx(s[n][e] - m_use[e >> 1]));
                     s[n][e] = p;
                     psum[e >> 1] += p;
                 }
@@ -553,7 +599,8 @@ template <typename T, int DQK, int DV, bool KV8 = false>
 cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, const Geo& g,
                    cudaStream_t s) {
     auto kern = prefix_mma_kernel<T, DQK, DV, KV8>;
-    const int smem = 1024 + g.stages * g.stage_bytes + g.nc * g.staging_bytes + 16 * g.stages;
+    const int smem = 1024 + g.stages * g.stage_bytes + g.nc * g.staging_bytes +
+                     g.nc * mma_query_smem_per_warp(DQK) + 16 * g.stages;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + 1) * 32), smem, s, kmap, vmap, a, g);

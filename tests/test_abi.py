@@ -191,3 +191,16 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load_library(str(tmp_path / "missing.so"))
         finally:
             binding._lib = saved
+
+
+def test_plan_head_dim_256_caps_consumer_warps(lib):
+    """At v_dim 256 a warp-level CTA runs at most 4 consumer warps (each keeps
+    a 16 x 256 fp32 accumulator in registers), and the query moves to shared
+    memory: the ring shrinks by 16 rows x 512 bytes per consumer warp."""
+    p = _plan(qk_dim=256, v_dim=256, num_q_heads=16, num_kv_heads=2, page_size=16)
+    assert p.path == va.VA_PATH_MMA and p.variant == 2 and p.heads_per_cta == 2
+    assert p.stages * p.stage_bytes + 4 * 16 * 512 <= 227 * 1024 - 2048
+    q = _plan(qk_dim=256, v_dim=256, num_q_heads=32, num_kv_heads=8, page_size=4)
+    assert q.path == va.VA_PATH_MMA and q.heads_per_cta * q.variant <= 4
+    with pytest.raises(va.VerifyAttnError):       # 5 m16 tiles per head > 4 consumers
+        _plan(qk_dim=256, v_dim=256, num_q_heads=80, num_kv_heads=4, page_size=4)
