@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // =================== softmax warps: thread = row ===================
             const int row = (warp & 3) * 32 + lane;              // TMEM lane quadrant = warp % 4
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-            float m_ref = -INFINITY, l_sum = 0.f;
+            float m_ref = -INFINITY, l_sum = 0.f, l_rnd = 0.f;
             SeqInfo si = {};
             int seg = -1;
             for (int k = 0; k < n_tiles; ++k) {
@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     si = a.seq[cur.b];
                     m_ref = -INFINITY;
                     l_sum = 0.f;
+                    l_rnd = 0.f;
                     ++seg;
                     // 0. this row's query chunks 0..5 into TMEM once the previous
                     //    segment's score MMAs are done with them
@@ -407,16 +408,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_ref = m_tile;
                 }
                 const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < kTok; ++j) {   // -inf (an invisible key) gives exactly 0
-                    // rounded to bf16 here, so the row sum is that of the weights
-                    // P V multiplies (the output stays a weighted mean)
-                    const float x = __bfloat162float(__float2bfloat16_rn(ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -mu))));
+                    const float x = ex2(fmaf(__uint_as_float(r[j]), a.scale_log2, -mu));
+                    // the weight rounded to bf16 as P V multiplies it: the output is
+                    // normalised by the sum of these (a weighted mean of V under the
+                    // weights applied), the log-sum-exp takes the exact sum
+                    const float xr = __bfloat162float(__float2bfloat16_rn(x));
                     ps4[j & 3] += x;
-                    r[j] = __float_as_uint(x);
+                    pr4[j & 3] += xr;
+                    r[j] = __float_as_uint(xr);
                 }
                 l_sum = l_sum * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+                l_rnd = l_rnd * alpha + ((pr4[0] + pr4[1]) + (pr4[2] + pr4[3]));
                 // 3. the previous P V must be done before P is rewritten or O rescaled
                 if (k >= 1) wait_fast(b_pvdone, (k - 1) & 1, 10, &abort_flag, hdr);
                 fence_after();
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (seg_end) {
                     wait_fast(b_pvdone, k & 1, 11, &abort_flag, hdr);
                     fence_after();
-                    const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;   // times the V dequant scale
+                    const float inv = l_rnd > 0.f ? a.v_scale / l_rnd : 0.f;   // times the V dequant scale
                     const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
                     float* po = a.part_o + (slot * kRows + row) * kV + rank * (kV / 2);
                     uint32_t r[32];

@@ -74,9 +74,6 @@ struct Mma<__nv_bfloat16> {
         __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
-    static __device__ __forceinline__ float round(float x) {
-        return __bfloat162float(__float2bfloat16_rn(x));
-    }
 };
 
 template <>
@@ -93,7 +90,6 @@ struct Mma<__half> {
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
-    static __device__ __forceinline__ float round(float x) { return __half2float(__float2half_rn(x)); }
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2,
@@ -517,9 +513,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             for (int n = 0; n < 2; ++n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    // rounded to the operand type here, so the row sum is that of
-                    // the weights P V multiplies (the output stays a weighted mean)
-                    const float p = Mma<MT>::round(ex2_approx(s[n][e] - m_use[e >> 1]));
+                    const float p = ex2_approx(s[n][e] - m_use[e >> 1]);
                     s[n][e] = p;
                     psum[e >> 1] += p;
                 }

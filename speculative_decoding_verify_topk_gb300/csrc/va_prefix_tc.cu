@@ -86,17 +86,6 @@ __device__ __forceinline__ uint32_t pack2(float x, float y) {
     }
 }
 
-// the two 16-bit values of a packed pair, summed in fp32
-template <typename T>
-__device__ __forceinline__ float sum2(uint32_t w) {
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-        return f.x + f.y;
-    }
-}
-
 template <typename T, int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -412,8 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // P = 2^(s - mu) into this tile's P buffer (K-major, 128-byte
                     // swizzle; row `row` = 64 tokens = 128 bytes) once the P V two
-                    // tiles back has read it; fp32 row sums of the rounded weights, so
-                    // the output is a weighted mean under the weights P V applies
+                    // tiles back has read it; fp32 row sums
                     if (k >= 2) wait_fast(b_pvdone + 8 * sb, ((k >> 1) - 1) & 1, 9, &abort_flag, hdr);
                     unsigned char* const prow = ps + sb * L::kPBytes + row * 128;
                     float sum4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -425,9 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // -inf (an invisible key) gives exactly 0
                             const float x0 = ex2(fmaf(__uint_as_float(r[8 * q + j]), a.scale_log2, -mu));
                             const float x1 = ex2(fmaf(__uint_as_float(r[8 * q + j + 1]), a.scale_log2, -mu));
+                            sum4[j >> 1] += x0 + x1;
                             pk[j >> 1] = pack2<T>(x0, x1);
-                            // the row sum of the rounded weights that P V multiplies
-                            sum4[j >> 1] += sum2<T>(pk[j >> 1]);
                         }
                         *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }

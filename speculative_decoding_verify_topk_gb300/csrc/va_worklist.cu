@@ -1,7 +1,8 @@
 // Work-list kernel: per-sequence facts for the prefix and combine kernels.
 //
-// One CTA of 1024 threads. For every sequence it checks the lengths and the
-// page-table capacity, derives the key range any row can see, [lo, P + D)
+// One CTA of up to 1024 threads (one per sequence). For every sequence it
+// checks the lengths and the page-table capacity, derives the key range any
+// row can see, [lo, P + D)
 // (the window's lowest bound belongs to row 0), counts its tiles, and takes
 // two exclusive prefix sums: query rows (qoff) and tiles (tile_off). The grid
 // of the later kernels depends only on host-known sizes; everything that
@@ -27,7 +28,7 @@ __device__ int block_exclusive_scan(int v, int* excl, int* warp_sums) {
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_sums[lane];
+        int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
     __syncthreads();
 
     int q_carry = 0, tile_carry = 0, err = 0;
-    for (int base = 0; base < a.bs; base += kThreads) {
+    for (int base = 0; base < a.bs; base += blockDim.x) {
         const int b = base + threadIdx.x;
         int qrows = 0, tiles = 0;
         SeqInfo si = {};
@@ -106,7 +107,10 @@ __global__ void __launch_bounds__(kThreads) worklist_kernel(Args a) {
 }  // namespace
 
 cudaError_t launch_worklist(const Args& a, cudaStream_t s) {
-    worklist_kernel<<<1, kThreads, 0, s>>>(a);
+    // one thread per sequence up to 1024 (a small batch then takes a single
+    // warp: the block-wide barriers of a 1024-thread block are most of its time)
+    const int threads = a.bs >= kThreads ? kThreads : ((a.bs + 31) / 32) * 32;
+    worklist_kernel<<<1, threads < 32 ? 32 : threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
