@@ -52,10 +52,11 @@ constexpr int kRows = 128;     // query rows per kv-head, padded (M of both MMAs
 // warps 4..7 hold rows 0..127; the producer and the MMA issuer sit on SM
 // sub-partitions 2 and 3, which they share with the softmax warps of rows
 // 64..127 (live only for more than 64 query rows per kv-head), so the
-// instruction stream of a busy softmax warp does not starve them. Warps 0 and
-// 1 only help initialise shared memory.
+// instruction stream of a busy softmax warp does not starve them. Warp 1
+// issues the P V MMAs (warp 3 the score MMAs); warp 0 only helps initialise
+// shared memory.
 constexpr int kThreads = 256;
-constexpr int kProducerWarp = 2, kMmaWarp = 3, kFirstSoftmaxWarp = 4;
+constexpr int kPvWarp = 1, kProducerWarp = 2, kMmaWarp = 3, kFirstSoftmaxWarp = 4;
 constexpr int kChunkBytes = kTok * 128;   // one 64-column chunk of a tile: [64 tokens][128 B]
 
 struct TcGeo {
@@ -203,24 +204,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = k0; k < n_tiles; ++k) mbar_wait(b_kfull + 8 * (k % geo.stages), (k / geo.stages) & 1);
             }
         } else if (warp == kMmaWarp) {
-            // =================== MMA issuer (one thread) ===================
-            // A fixed software pipeline: the scores of tile k + 1 go to the
-            // tensor cores before P V of tile k, so they are ready when the
-            // softmax finishes tile k. When tile k + 1 opens a segment its query
-            // is written only after tile k's partial output has been read, which
-            // needs P V of tile k: then P V goes first.
+            // =================== score MMA issuer (one thread) ===================
+            // S of tile k once its stage has landed and the softmax has read the
+            // S buffer two tiles back; at a segment start, once the softmax warps
+            // have written the segment's query. A second thread (warp kPvWarp)
+            // issues P V: an issuing thread waits about as long as each MMA
+            // takes, so one thread issuing both kinds paced the whole tile.
             if (lane == 0) {
                 constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
                 const uint32_t id_s = idesc_f16(kRows, kTok, 0, 0, kBf16);
-                const uint32_t id_o = idesc_f16(kRows, DV, 0, 1, kBf16);
-                const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
-                Cursor qk_cur = cur, pv_cur = cur;
                 int qk_seg = -1;
-                auto issue_qk = [&](int k) {
+                for (int k = 0; k < n_tiles && !*(volatile int*)&abort_flag; ++k) {
                     // S = Q K^T  (M 128, N 64 tokens, K = Dqk in steps of 16)
                     const int st = k % geo.stages, sb = k & 1;
-                    const bool seg_begin = (k == 0) || (qk_cur.t == 0);
-                    const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
+                    const bool seg_begin = (k == 0) || (cur.t == 0);
+                    const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
                     if (seg_begin) wait_fast(b_qfull, (++qk_seg) & 1, 3, &abort_flag, hdr);
                     wait_fast(b_kfull + 8 * st, (k / geo.stages) & 1, 4, &abort_flag, hdr);
                     if (k >= 2) wait_fast(b_sfree + 8 * sb, ((k >> 1) - 1) & 1, 5, &abort_flag, hdr);
@@ -234,19 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     k_desc + (uint64_t)((c * kChunkBytes + s4 * 32) >> 4), id_s, (c | s4) != 0);
                     umma_commit(b_sfull + 8 * sb);
                     if (seg_end) umma_commit(b_qfree);   // the segment's query is no longer read
-                    if (k + 1 < n_tiles) qk_cur.advance(a);
-                };
-                // One action per pass: the scores of tile q (q <= k + 1) unless q
-                // is the next tile and opens a segment, else P V of tile k.
-                int q = 0;
-                for (int k = 0; k < n_tiles;) {
-                    if (q < n_tiles && q <= k + 1 && (q == k || qk_cur.t != 0)) {
-                        issue_qk(q++);
-                        continue;
-                    }
+                    if (k + 1 < n_tiles) cur.advance(a);
+                }
+                // this thread's last commits have landed before the CTA may exit
+                wait_fast(b_sfull + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, 13, &abort_flag, hdr);
+            }
+        } else if (warp == kPvWarp) {
+            // =================== P V issuer (one thread) ===================
+            // P V of tile k once the softmax has written its P (and rescaled O);
+            // its commit releases the stage (the scores of tile k were read
+            // before P was written).
+            if (lane == 0) {
+                constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+                const uint32_t id_o = idesc_f16(kRows, DV, 0, 1, kBf16);
+                const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
+                for (int k = 0; k < n_tiles && !*(volatile int*)&abort_flag; ++k) {
                     // O += P V  (M 128, N Dv, K 64 tokens; V token-major)
                     const int st = k % geo.stages;
-                    const bool first = (k == 0) || (pv_cur.t == 0);
+                    const bool first = (k == 0) || (cur.t == 0);
                     wait_fast(b_pfull + 8 * (k & 1), (k >> 1) & 1, 6, &abort_flag, hdr);
                     fence_after();
                     const uint64_t pk = p_desc + (uint64_t)(((k & 1) * L::kPBytes) >> 4);
@@ -258,8 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              !(first && s4 == 0));
                     umma_commit(b_pvdone + 8 * (k & 1));
                     umma_commit(b_kempty + 8 * st);
-                    if (k + 1 < n_tiles) pv_cur.advance(a);
-                    ++k;
+                    if (k + 1 < n_tiles) cur.advance(a);
                 }
                 // the last commits have landed before the CTA may exit
                 wait_fast(b_pvdone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, 12, &abort_flag, hdr);
