@@ -152,50 +152,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kProducerWarp) {
             // =================== TMA producer (one warp) ===================
             // Lane 0 waits for the stage and posts the byte count; then lane q
-            // resolves the page of the tile's box q0 + q and issues its copies,
-            // so the boxes of a tile go out in parallel.
+            // issues the copies of the tile's box q0 + q, so the boxes of a tile
+            // go out in parallel. Each lane reads its box's page id two tiles
+            // ahead: the page table is cold in L2 at the start of a call, and a
+            // read on the issue path held every tile for its DRAM latency.
             const int tb_log2 = __ffs(geo.tb) - 1;   // boxes are 2^tb_log2 tokens
             const uint32_t box_bytes = (uint32_t)(L::kQc + L::kVc) * geo.tb * 128;
+            struct Boxes {
+                int g, boxes, q, page, j;   // kv-head, boxes of the tile, this lane's box, its page and first token
+            };
             int b_seen = -1, indptr = 0;
             SeqInfo si = {};
-            for (int k = 0; k < n_tiles; ++k) {
-                const int st = k % geo.stages;
-                if (cur.b != b_seen) {
-                    si = a.seq[cur.b];
-                    indptr = __ldg(a.kv_indptr + cur.b);
-                    b_seen = cur.b;
+            // the boxes of the tile at cursor c that overlap the keys [lo, P + D),
+            // and the page of this lane's box (issued now, used two tiles later)
+            auto resolve = [&](const Cursor& c) {
+                if (c.b != b_seen) {
+                    si = a.seq[c.b];
+                    indptr = __ldg(a.kv_indptr + c.b);
+                    b_seen = c.b;
                 }
-                // the boxes [q0, q1) of the tile that overlap the keys [lo, P + D)
-                const int j0 = si.a0 + cur.t * kTok;
+                const int j0 = si.a0 + c.t * kTok;
                 const int end = si.prefix + si.draft;
                 const int q0 = si.lo > j0 ? (si.lo - j0) >> tb_log2 : 0;
                 int q1 = end < j0 + kTok ? (end - j0 + geo.tb - 1) >> tb_log2 : kTok >> tb_log2;
                 if (q1 < q0) q1 = q0;
+                Boxes r;
+                r.g = c.g;
+                r.boxes = q1 - q0;
+                r.q = q0 + lane;
+                r.j = j0 + (r.q << tb_log2);
+                r.page = r.q < q1 ? __ldg(a.page_table + indptr + r.j / a.page_size) : 0;
+                return r;
+            };
+            auto issue_tile = [&](int k, const Boxes& cb) {
+                const int st = k % geo.stages;
                 if (lane == 0) {
                     if (k >= geo.stages)
                         wait_fast(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2, &abort_flag, hdr);
-                    mbar_arrive_expect_tx(b_kfull + 8 * st, (uint32_t)(q1 - q0) * box_bytes);
+                    mbar_arrive_expect_tx(b_kfull + 8 * st, (uint32_t)cb.boxes * box_bytes);
                 }
                 __syncwarp();
-                const int q = q0 + lane;
-                if (q < q1) {
+                if (lane < cb.boxes) {
                     const uint32_t stg = smem_u32(ring + st * geo.stage_bytes);
-                    const int j = j0 + (q << tb_log2);
-                    const int page = __ldg(a.page_table + indptr + j / a.page_size);
+                    const int page = cb.page;
                     if (page < 0 || page >= a.num_pages) set_error(a, VA_ERR_BAD_PAGE);
                     // an out-of-range id still delivers its bytes (from page 0) so the count balances
-                    const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size + j % a.page_size;
-                    const uint32_t dst = stg + (uint32_t)(q << tb_log2) * 128;
+                    const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size + cb.j % a.page_size;
+                    const uint32_t dst = stg + (uint32_t)(cb.q << tb_log2) * 128;
 #pragma unroll
                     for (int c = 0; c < L::kQc; ++c)
-                        tma_3d(dst + c * kChunkBytes, &kmap, c * 64, slot, cur.g, b_kfull + 8 * st);
+                        tma_3d(dst + c * kChunkBytes, &kmap, c * 64, slot, cb.g, b_kfull + 8 * st);
 #pragma unroll
                     for (int c = 0; c < L::kVc; ++c)
-                        tma_3d(dst + (L::kQc + c) * kChunkBytes, &vmap, c * 64, slot, cur.g, b_kfull + 8 * st);
+                        tma_3d(dst + (L::kQc + c) * kChunkBytes, &vmap, c * 64, slot, cb.g, b_kfull + 8 * st);
                 }
                 // the combine may launch while this CTA drains its ring
                 if (k + 1 == n_tiles && lane == 0) pdl_launch_dependents();
-                if (k + 1 < n_tiles) cur.advance(a);
+            };
+            // two register sets, for even and odd tiles: the page read of tile
+            // k + 2 lands in the set tile k has just used, with no copies between
+            Cursor ahead = cur;
+            Boxes b_even = resolve(ahead), b_odd = {};
+            if (n_tiles > 1) {
+                ahead.advance(a);
+                b_odd = resolve(ahead);
+            }
+            for (int k = 0; k < n_tiles; k += 2) {
+                issue_tile(k, b_even);
+                if (k + 2 < n_tiles) {
+                    ahead.advance(a);
+                    b_even = resolve(ahead);
+                }
+                if (k + 1 < n_tiles) {
+                    issue_tile(k + 1, b_odd);
+                    if (k + 3 < n_tiles) {
+                        ahead.advance(a);
+                        b_odd = resolve(ahead);
+                    }
+                }
             }
             // Normally the MMAs consume every fill before the CTA ends. After an
             // abort, wait (bounded) for the last fill of each stage.
