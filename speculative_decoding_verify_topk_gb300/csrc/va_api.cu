@@ -309,6 +309,7 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.tile = plan->tile_tokens;
     a.hg = plan->heads_per_cta;
     a.mla = plan->path == VA_PATH_MLA;
+    a.direct_whole = plan->path == VA_PATH_TC;
     if (a.hg < 1 || p.num_kv_heads % a.hg != 0) return VA_INVALID_ARG;
     a.scale = scale;
     a.scale_log2 = scale * k_scale * 1.4426950408889634f;

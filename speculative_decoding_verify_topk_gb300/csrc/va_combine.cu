@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
     }
     const int c_first = cta_of_tile(x0, work, workers);
     const int c_last = cta_of_tile(x0 + si.tiles - 1, work, workers);
+    // one CTA covered the pair alone: it wrote the final rows itself
+    if (a.direct_whole && c_first == c_last) return;
     const bool all_busy = work >= workers;   // then every worker got at least one tile
     // This warp's segments: workers c_first + part + W j. Whether worker c
     // covered some tile (more workers than tiles leaves some idle) is evaluated

@@ -80,6 +80,8 @@ struct Args {
     int hg;                  // kv-heads a prefix CTA handles together (1 on the fp32 path)
     int mla;                 // 1: absorbed-MLA layout (row blocks of 128 heads per draft,
                              //    2-CTA clusters, partial slots of 128 rows)
+    int direct_whole;        // 1: the prefix kernel writes the final rows of a (kv-head,
+                             //    sequence) that one CTA covers alone; the combine skips it
     float scale_log2;        // scale * k_scale * log2(e)
     float scale;
     float v_scale;           // per-tensor V dequantisation scale (1 unless a quantised cache)

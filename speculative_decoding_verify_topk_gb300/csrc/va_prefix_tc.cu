@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the arithmetic but keeps every wait and arrival in step.
             bool wlive = true;
             bool rows_live = false;   // this thread's row is a query row of the segment
+            bool seg_whole = false;   // the segment holds every tile of its (kv-head, sequence)
             for (int k = 0; k < n_tiles; ++k) {
                 const int sb = k & 1;
                 const bool seg_begin = (k == 0) || (cur.t == 0);
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_ref = -INFINITY;
                     l_sum = 0.f;
                     ++seg;
+                    seg_whole = cur.t == 0;   // and, at its end, t == tiles - 1
                     rows_b = a.group * si.draft;
                     rows_live = row < rows_b;
                     const int i = row / a.group, hh = row - i * a.group;
@@ -478,10 +480,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_before();
                 mbar_arrive(b_pfull + 8 * sb);
                 // segment end: the normalised partial output, times the V scale
+                // (or the final rows, when the segment is the whole pair)
                 if (seg_end) {
                     wait_fast(b_pvdone + 8 * sb, (k >> 1) & 1, 11, &abort_flag, hdr);
                     fence_after();
-                    if (wlive) {
+                    if (wlive && seg_whole && cur.t == cur.tiles - 1) {
+                        // this CTA covered the (kv-head, sequence) alone: the
+                        // final row (output type, natural-log lse), no partial
+                        const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;
+                        const int i = row / a.group, hh = row - i * a.group;
+                        const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + g * a.group + hh;
+                        T* og = reinterpret_cast<T*>(a.out) + qrow * DV;
+                        uint32_t r[32];
+#pragma unroll 1
+                        for (int c = 0; c < DV; c += 32) {
+                            VA_TC_LD32(t_o + c + lane_off, r);
+                            tmem_wait_ld();
+                            if (rows_live) {
+#pragma unroll
+                                for (int j = 0; j < 32; j += 8)
+                                    *reinterpret_cast<uint4*>(og + c + j) = make_uint4(
+                                        pack2<T>(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv),
+                                        pack2<T>(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv),
+                                        pack2<T>(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv),
+                                        pack2<T>(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv));
+                            }
+                        }
+                        if (rows_live)
+                            a.lse[qrow] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+                    } else if (wlive) {
                         const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;
                         const int64_t slot = partial_slot(a, g, cur.b, cta);
                         float* po = a.part_o + (slot * a.rows_cap + row) * DV;
