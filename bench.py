@@ -213,7 +213,7 @@ def stored_profile(kernel: str, workload: str) -> dict:
     for line in open(path):
         line = line.strip()
         if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_digest",
-                                            "tensor_pipe_active_pct")):
+                                            "tensor_pipe_active_pct", "captured_algorithmic_bytes")):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("source_digest") != kernel_digest(kernel):
@@ -225,6 +225,10 @@ def stored_profile(kernel: str, workload: str) -> dict:
         pass
     try:
         out["tensor_pipe_active_pct"] = float(fields["tensor_pipe_active_pct"])
+    except (KeyError, ValueError):
+        pass
+    try:   # the algorithmic bytes of the captured launch, when its call differs from the average one
+        out["captured_algorithmic_bytes"] = int(float(fields["captured_algorithmic_bytes"]))
     except (KeyError, ValueError):
         pass
     return out
@@ -658,8 +662,13 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
     prof = stored_profile(kernel, wl.name)
     prefix_bytes = sum(accts[win(i)]["prefix_bytes"] for i in range(prof_steps))
     achieved = prefix_bytes / (sum(prefix_ms) * 1e-3) / 1e9
+    traffic = prof.get("traffic")
+    if traffic is not None and prof.get("captured_algorithmic_bytes"):
+        # the capture took one window's call; per launch here means averaged over the
+        # steps' windows, so scale by the algorithmic bytes (DRAM traffic follows them)
+        traffic = int(traffic * mean_of("prefix_bytes", prof_steps) / prof["captured_algorithmic_bytes"])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": prof.get("traffic"), "kernel": kernel,
+                "frac": achieved / hbm_peak, "traffic": traffic, "kernel": kernel,
                 "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": mean_of("prefix_bytes", prof_steps),
