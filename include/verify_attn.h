@@ -134,7 +134,8 @@ typedef struct va_plan {
     int32_t box_tokens;       /* tokens per bulk-tensor copy (gcd(page_size, tile_tokens)) */
     int32_t stages;           /* shared-memory ring depth of the prefix kernel */
     int32_t stage_bytes;      /* bytes per ring stage */
-    uint64_t reserved[2];
+    uint64_t off_chunks;      /* byte offset of the combine's work list inside the workspace */
+    uint64_t reserved;
 } va_plan;
 
 /*

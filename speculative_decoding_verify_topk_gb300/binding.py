@@ -45,7 +45,7 @@ class Plan(ctypes.Structure):
                 ("off_part_lse", ctypes.c_uint64), ("off_part_o", ctypes.c_uint64),
                 ("heads_per_cta", ctypes.c_int32), ("box_tokens", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
-                ("reserved", ctypes.c_uint64 * 2)]
+                ("off_chunks", ctypes.c_uint64), ("reserved", ctypes.c_uint64)]
 
 
 class VerifyAttnError(RuntimeError):

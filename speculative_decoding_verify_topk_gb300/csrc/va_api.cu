@@ -124,7 +124,6 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     if (kv8 && (p.dtype == VA_FP32 || p.v_aliases_k || p.qk_dim % 128 || p.v_dim % 128))
         return VA_UNSUPPORTED;
     if (p.v_aliases_k && p.v_dim > p.qk_dim) return VA_INVALID_ARG;
-    if ((int64_t)p.max_bs * p.num_kv_heads > 65535) return VA_UNSUPPORTED;   // combine grid.y
     if (!va::combine_supported(p.qk_dim, p.v_dim)) return VA_UNSUPPORTED;
 
     va_plan out;
@@ -236,6 +235,10 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
     size_t off = align_up(va::kHeaderBytes);
     out.off_seq = off;
     off = align_up(off + sizeof(va::SeqInfo) * (size_t)p.max_bs);
+    // the combine's work list: one entry per (stream, sequence) pair, plus the total
+    const int64_t streams = out.path == VA_PATH_MLA ? p.max_draft : p.num_kv_heads / out.heads_per_cta;
+    out.off_chunks = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)(streams * p.max_bs + 1));
     out.off_part_lse = off;
     off = align_up(off + sizeof(float) * (size_t)slots * slot_rows);
     out.off_part_o = off;
@@ -309,8 +312,21 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
     a.tile = plan->tile_tokens;
     a.hg = plan->heads_per_cta;
     a.mla = plan->path == VA_PATH_MLA;
-    a.direct_whole = plan->path == VA_PATH_TC;
+    a.dtype = p.dtype;
+    a.chunk_off = reinterpret_cast<int32_t*>(ws + plan->off_chunks);
     if (a.hg < 1 || p.num_kv_heads % a.hg != 0) return VA_INVALID_ARG;
+    // Combine chunk: with about `segs` segments per split pair (the workers
+    // spread over the pairs, or two when the pairs outnumber them), W warps per
+    // row -- the smallest power of two up to 8 that leaves each warp at most one
+    // batch of 8 partial rows -- and rpc = 8 / W rows per chunk.
+    {
+        const int64_t pairs = (int64_t)bs * va::stream_count(a);
+        const int workers = va::worker_count(a);
+        const int64_t segs = pairs >= workers ? 2 : workers / pairs + 1;
+        int w = 1;
+        while (w < 8 && (int64_t)w * 8 < segs) w *= 2;
+        a.rpc = 8 / w;
+    }
     a.scale = scale;
     a.scale_log2 = scale * k_scale * 1.4426950408889634f;
     a.v_scale = v_scale;

@@ -10,14 +10,14 @@
 //   Z = sum_c 2^(lse_c - M),  o = sum_c 2^(lse_c - M) o_c / Z,
 //   lse = (M + log2 Z) ln 2          (natural log, as the header promises).
 //
-// One warp per query row, or W warps per row when few rows each merge many
-// segments (grid: blocks of 8 / W rows x (bs * Hkv)). Lane l owns the output
-// columns [l * VPL, (l + 1) * VPL), so every partial row is read as one
-// coalesced run. The segments' lse values (lane-parallel) and the first batch
-// of partial rows are loaded in one round -- no load waits on a weight -- and
-// the rest in batches. The sequence table and tile count come from the work
-// list, which finished before the prefix kernel started its work, so they are
-// read before the wait.
+// Only the pairs a worker boundary splits have partials: a pair one worker
+// covers alone was written whole by the prefix kernel, and a failed sequence
+// by the work-list kernel, which also lists the split pairs' row chunks. The
+// grid is persistent over that list (its length is known on the device
+// only). Lane l owns the output columns [l * VPL, (l + 1) * VPL), so every
+// partial row is read as one coalesced run; the segments' lse values
+// (lane-parallel) and the first batch of partial rows are loaded in one round
+// -- no load waits on a weight -- and the rest in batches.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,15 +29,6 @@ namespace va {
 namespace {
 
 constexpr int kWarps = 8;
-
-template <typename T>
-__device__ __forceinline__ T from_f32(float v);
-template <>
-__device__ __forceinline__ float from_f32<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
-template <>
-__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 
 // VPL consecutive floats of a row, vectorised.
 template <int VPL>
@@ -89,72 +80,23 @@ __device__ __forceinline__ void store_row(T* og, const float (&acc)[VPL], float 
     }
 }
 
-// VPL = v_dim / 32 output columns per lane (compile-time: the loops below
-// carry no predicates). A block of kWarps warps serves kWarps / W rows; the W
-// warps of one row split the row's segments (warp p takes segments p, p + W,
-// ...) and merge their partial sums through shared memory. W > 1 when a few
-// (kv-head, sequence) pairs are each split over many CTAs (one long sequence
-// over the whole grid): one warp per row would walk a long chain of dependent
-// load rounds.
+// Merges one output row from the partials of workers c_first .. c_last.
+// VPL = v_dim / 32 output columns per lane (compile-time: the loops carry no
+// predicates). W warps serve the row: warp `part` takes segments part,
+// part + W, ... and the W merge their sums through shared memory (named
+// barrier 1 + rs among the row's warps); W > 1 when a row merges many segments
+// (one long sequence over the whole grid), where one warp would walk a long
+// chain of dependent load rounds.
 template <typename T, int VPL>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
-    __shared__ float sm_m[kWarps];
-    __shared__ float sm_z[kWarps];
-    __shared__ __align__(16) float sm_acc[kWarps][32 * VPL];
+__device__ __forceinline__ void merge_row(const Args& a, int W, int part, int rs, int c_first, int c_last,
+                                          int64_t work, int workers, int64_t slot0, int64_t slot_rows,
+                                          int64_t prow, T* og, float* lse_out, float* sm_m, float* sm_z,
+                                          float (*sm_acc)[32 * VPL]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rpb = kWarps / W, rs = warp / W, part = warp - rs * W;
-    const int bg = blockIdx.y;
-    const int b = bg / a.hkv, g = bg - b * a.hkv;
-    // The work list finished before the prefix kernel began its work, so its
-    // sequence table is complete here; only the partials need the wait.
-    const SeqInfo si = a.seq[b];
-    const int total_tiles = a.header[kHdrTotalTiles];
-    const int rows_b = a.group * si.draft;
-    const int r = blockIdx.x * rpb + rs;   // the W warps of a row share r and leave together
-    pdl_wait();   // partials of the prefix kernel are ready
-    if (r >= rows_b) return;
-    const int i = r / a.group, h = g * a.group + (r - i * a.group);
-    const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + h;
-    T* og = reinterpret_cast<T*>(a.out) + qrow * (VPL * 32) + lane * VPL;
-    if (si.bad || si.tiles == 0) {
-        if (part == 0) {
-#pragma unroll
-            for (int e = 0; e < VPL; ++e) og[e] = from_f32<T>(NAN);
-            if (lane == 0) a.lse[qrow] = NAN;
-        }
-        return;
-    }
-
-    // ---- the segments that covered this row: workers c_first .. c_last of the
-    // partition. GQA: the stream is over (head group, sequence, tile) and the
-    // workers are CTAs; MLA: over (row block = draft, sequence, tile) and the
-    // workers are 2-CTA clusters, whose slots hold 128 rows.
-    int64_t work, x0, slot0, slot_rows, prow;
-    int workers;
-    if (a.mla) {
-        workers = a.num_ctas / 2;
-        work = (int64_t)a.max_draft * total_tiles;
-        x0 = (int64_t)i * total_tiles + si.tile_off;
-        slot0 = (int64_t)i * (a.bs + workers) + b;
-        slot_rows = 128;
-        prow = h;
-    } else {
-        workers = a.num_ctas;
-        work = (int64_t)(a.hkv / a.hg) * total_tiles;
-        x0 = (int64_t)(g / a.hg) * total_tiles + si.tile_off;
-        slot0 = partial_slot(a, g, b, 0);   // slot of CTA c is slot0 + c
-        slot_rows = a.rows_cap;
-        prow = r;
-    }
-    const int c_first = cta_of_tile(x0, work, workers);
-    const int c_last = cta_of_tile(x0 + si.tiles - 1, work, workers);
-    // one CTA covered the pair alone: it wrote the final rows itself
-    if (a.direct_whole && c_first == c_last) return;
     const bool all_busy = work >= workers;   // then every worker got at least one tile
     // This warp's segments: workers c_first + part + W j. Whether worker c
     // covered some tile (more workers than tiles leaves some idle) is evaluated
-    // once per lane and shared as a ballot word, so the division sits in the
-    // code once.
+    // once per lane and shared as a ballot word.
     const int stride = W * 32;
     auto live_word = [&](int cb) {   // workers cb + W l for lanes l
         const int c = cb + W * lane;
@@ -162,14 +104,14 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
         return __ballot_sync(0xffffffffu, live);
     };
     auto lse_of = [&](int c) { return a.part_lse[(slot0 + c) * slot_rows + prow]; };
+    auto row_ptr = [&](int c) {
+        return a.part_o + ((slot0 + c) * slot_rows + prow) * (VPL * 32) + lane * VPL;
+    };
 
     // ---- one round of independent loads: the segments' lse values (lane l
     // holds segment c0 + W l) and the first batch of partial rows; only then
     // the max, the weights and the sums
     constexpr int kBatch = VPL <= 8 ? 8 : 4;   // partial rows in flight per round
-    auto row_ptr = [&](int c) {
-        return a.part_o + ((slot0 + c) * slot_rows + prow) * (VPL * 32) + lane * VPL;
-    };
     const int c0 = c_first + part;
     const uint32_t live0 = live_word(c0);
     const float lse_first = (live0 >> lane) & 1u ? lse_of(c0 + W * lane) : -INFINITY;
@@ -179,7 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
         if ((live0 >> u) & 1u) load_f32<VPL>(row_ptr(c0 + W * u), v[u]);
     float mx = lse_first;
 #pragma unroll 1
-    for (int cb = c0 + stride; cb <= c_last; cb += stride) {   // more than 32 segments per warp: rare
+    for (int cb = c0 + stride; cb <= c_last; cb += stride) {   // more than 32 segments per warp
         const uint32_t lw = live_word(cb);
         if ((lw >> lane) & 1u) mx = fmaxf(mx, lse_of(cb + W * lane));
     }
@@ -223,7 +165,6 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
 
     if (W > 1) {
         // ---- merge the W warps of this row: rescale each to the row's max
-        // (named barrier 1 + rs among the row's W warps)
         if (lane == 0) sm_m[warp] = mx;
         named_bar_sync(1 + rs, W * 32);
         float m_row = -INFINITY;
@@ -248,27 +189,100 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Args a, int W) {
     }
     // z == 0: the row sees no key at all (tree verify over an empty prefix with
     // no draft bit set); its output is zeros and its lse -inf
-    store_row<T, VPL>(og, acc, z > 0.f ? 1.f / z : 0.f);
-    if (lane == 0) a.lse[qrow] = z > 0.f ? (mx + __log2f(z)) * 0.69314718055994531f : -INFINITY;
+    store_row<T, VPL>(og + lane * VPL, acc, z > 0.f ? 1.f / z : 0.f);
+    if (lane == 0) *lse_out = z > 0.f ? (mx + __log2f(z)) * 0.69314718055994531f : -INFINITY;
 }
 
-// Warps per row: about one per eight segments of an average row (a
-// (kv-head or row block, sequence) pair is covered by about
-// workers / (pairs' streams) + 1 segments), as a power of two up to 8.
-int warps_per_row(const Args& a) {
-    const int workers = a.mla ? a.num_ctas / 2 : a.num_ctas;
-    const int64_t streams = (int64_t)a.bs * (a.mla ? a.max_draft : a.hkv / a.hg);
-    const int64_t cover = (workers + streams - 1) / streams + 1;
-    int w = 1;
-    while (w < kWarps && (int64_t)w * 8 < cover) w *= 2;
-    return w;
+// Blocks per SM the register budget must allow: the CTAs are short, so more
+// resident ones beat the last few registers of a wide row.
+constexpr int combine_min_blocks(int vpl) { return vpl >= 8 ? 2 : 3; }
+
+// The largest p in [0, n) with off[p] <= q, for a non-decreasing off with
+// off[0] <= q: the pair whose chunks include chunk q (pairs without chunks
+// share their offset with the next and are passed over). Warp-cooperative:
+// each round probes 32 evenly spaced entries in one load.
+__device__ __forceinline__ int find_pair(const int32_t* off, int n, int q) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int probe = lo + lane * step;
+        const uint32_t m = __ballot_sync(0xffffffffu, probe < hi && __ldg(off + probe) <= q);
+        lo += (31 - __clz(m)) * step;   // the passing lanes form a prefix
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
+// Persistent over the work list the work-list kernel built: chunk q is rpc
+// consecutive rows of one split pair, merged by W = 8 / rpc warps per row.
+// Pairs one worker covered alone are not in the list (the prefix kernel wrote
+// their rows), nor are failed sequences (the work-list kernel wrote NaN).
+template <typename T, int VPL>
+__global__ void __launch_bounds__(kWarps * 32, combine_min_blocks(VPL)) combine_kernel(Args a) {
+    __shared__ float sm_m[kWarps];
+    __shared__ float sm_z[kWarps];
+    __shared__ __align__(16) float sm_acc[kWarps][32 * VPL];
+    const int warp = threadIdx.x >> 5;
+    const int workers = worker_count(a), streams = stream_count(a);
+    // The work list finished before the prefix kernel began its work, so its
+    // tables are complete here; only the partials need the wait.
+    const int total_tiles = a.header[kHdrTotalTiles];
+    const int n_chunks = a.header[kHdrChunks];
+    const int64_t work = (int64_t)streams * total_tiles;
+    const int n_pairs = streams * a.bs;
+    const int W = kWarps / a.rpc;
+    const int rs = warp / W, part = warp - rs * W;
+    bool waited = false;
+    for (int q = blockIdx.x; q < n_chunks; q += gridDim.x) {   // block-uniform
+        const int p = find_pair(a.chunk_off, n_pairs, q);
+        const int b = p / streams, g = p - b * streams;   // sequence, stream
+        const SeqInfo si = a.seq[b];
+        const int64_t x0 = (int64_t)g * total_tiles + si.tile_off;
+        const int c_first = cta_of_tile(x0, work, workers);
+        const int c_last = cta_of_tile(x0 + si.tiles - 1, work, workers);
+        const int rows_b = a.group * si.draft;   // rows of one kv-head (GQA)
+        const int R = a.mla ? a.hq : a.hg * rows_b;
+        const int f = (q - __ldg(a.chunk_off + p)) * a.rpc + rs;   // row of the pair
+        if (!waited) {
+            pdl_wait();   // partials of the prefix kernel are ready
+            waited = true;
+        }
+        if (f < R) {
+            int64_t slot0, slot_rows, prow, qrow;
+            if (a.mla) {   // row block g = draft index, f = head
+                slot0 = (int64_t)g * (a.bs + workers) + b;
+                slot_rows = a.hq;
+                prow = f;
+                qrow = (int64_t)(si.qoff + g) * a.hq + f;
+            } else {       // f = (head in the group, row of that kv-head)
+                const int gl = f / rows_b, r = f - gl * rows_b;
+                const int h = g * a.hg + gl;   // kv-head
+                const int i = r / a.group, hh = r - i * a.group;
+                slot0 = partial_slot(a, h, b, 0);   // slot of worker c is slot0 + c
+                slot_rows = a.rows_cap;
+                prow = r;
+                qrow = (int64_t)(si.qoff + i) * a.hq + h * a.group + hh;
+            }
+            merge_row<T, VPL>(a, W, part, rs, c_first, c_last, work, workers, slot0, slot_rows, prow,
+                              reinterpret_cast<T*>(a.out) + qrow * (VPL * 32), a.lse + qrow, sm_m, sm_z,
+                              sm_acc);
+        }
+        if (W > 1) __syncthreads();   // the shared sums are free again
+    }
 }
 
 template <typename T, int VPL>
 cudaError_t launch_t(const Args& a, cudaStream_t s) {
-    const int W = warps_per_row(a), rpb = kWarps / W;
-    dim3 grid((a.rows_cap + rpb - 1) / rpb, a.bs * a.hkv);
-    return launch_pdl(combine_kernel<T, VPL>, grid, dim3(kWarps * 32), 0, s, a, W);
+    const int workers = worker_count(a);
+    if (workers < 2) return cudaSuccess;   // one worker covers every pair whole
+    // at most workers - 1 split pairs (a boundary splits one pair at most), each
+    // of at most R_max rows; a grid of the CTAs that fit on the SMs at once
+    const int64_t r_max = a.mla ? a.hq : (int64_t)a.hg * a.rows_cap;
+    const int64_t bound = (int64_t)(workers - 1) * ((r_max + a.rpc - 1) / a.rpc);
+    const int64_t resident = (int64_t)combine_min_blocks(VPL) * a.num_ctas;
+    const int64_t grid = bound < resident ? bound : resident;
+    return launch_pdl(combine_kernel<T, VPL>, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, a);
 }
 
 template <typename T>

@@ -19,17 +19,24 @@
 //     contiguous stream range [c * H * T / N, (c + 1) * H * T / N). Every
 //     CTA thus streams the same number of KV bytes whatever the length mix.
 //   * A maximal run of one CTA's tiles that belongs to one (g, b) is a
-//     segment. It writes one normalised partial output and its base-2
+//     segment. A segment that holds every tile of its (g, b) is the whole
+//     answer: the prefix kernel writes the final rows itself. Any other
+//     segment writes one normalised partial output and its base-2
 //     log-sum-exp to slot g * bs + b + c; along the stream these slot ids
 //     strictly increase, so they are unique and those of one (g, b) are
-//     contiguous in c. The combine finds the CTAs that cover a (g, b) from the
-//     same partition formula.
+//     contiguous in c. Only a CTA boundary can split a (g, b), so the combine
+//     runs one CTA per boundary: the boundary's (g, b) and its segments follow
+//     from the same partition formula.
 #pragma once
 
 #include <cuda.h>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "../../include/verify_attn.h"
 
@@ -40,7 +47,7 @@ constexpr int kMaxDraft = 32;      // largest supported num_draft (one lane per 
 constexpr int kHeaderBytes = 256;  // workspace header: error word, totals
 
 // Header words (int32) at the start of the workspace.
-enum HeaderWord { kHdrError = 0, kHdrTotalTiles = 1, kHdrBs = 2, kHdrWaitSites = 3 };
+enum HeaderWord { kHdrError = 0, kHdrTotalTiles = 1, kHdrBs = 2, kHdrWaitSites = 3, kHdrChunks = 4 };
 
 // Per-sequence facts computed by the work-list kernel (32 bytes).
 struct SeqInfo {
@@ -70,6 +77,9 @@ struct Args {
     SeqInfo* seq;            // [max_bs]
     float* part_lse;         // [num_slots * rows_cap]   base-2 lse of each partial row
     float* part_o;           // [num_slots * rows_cap * v_dim]
+    int32_t* chunk_off;      // [bs * streams + 1] combine work list: exclusive scan, over the
+                             // pairs b * streams + g, of the row chunks of the pairs a worker
+                             // boundary splits (0 for the others)
     int64_t num_pages;
     int64_t max_kv_len;
     int64_t k_row_stride;    // elements between consecutive (slot, head) rows of K
@@ -80,8 +90,8 @@ struct Args {
     int hg;                  // kv-heads a prefix CTA handles together (1 on the fp32 path)
     int mla;                 // 1: absorbed-MLA layout (row blocks of 128 heads per draft,
                              //    2-CTA clusters, partial slots of 128 rows)
-    int direct_whole;        // 1: the prefix kernel writes the final rows of a (kv-head,
-                             //    sequence) that one CTA covers alone; the combine skips it
+    int dtype;               // VA_FP32 / VA_BF16 / VA_FP16: the element type of q and out
+    int rpc;                 // rows per combine chunk (1, 2, 4 or 8; 8 / rpc warps per row)
     float scale_log2;        // scale * k_scale * log2(e)
     float scale;
     float v_scale;           // per-tensor V dequantisation scale (1 unless a quantised cache)
@@ -162,6 +172,30 @@ cudaError_t launch_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, c
 // Device helpers
 // ---------------------------------------------------------------------------
 
+// Two output values as one 32-bit word of 16-bit elements (x in the low half).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+    static_assert(std::is_same<T, __nv_bfloat16>::value || std::is_same<T, __half>::value, "16-bit T");
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(x, y);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// A 32-bit word of quiet NaNs of the output type (one fp32, or two 16-bit values).
+__device__ __forceinline__ uint32_t nan_word(int dtype) {
+    return dtype == VA_FP32 ? 0x7fc00000u : dtype == VA_BF16 ? 0x7fc07fc0u : 0x7e007e00u;
+}
+
+// Base-2 log-sum-exp of a row (running max m, sum of weights l) as the
+// natural-log value the API returns; -inf for a row that saw no key.
+__device__ __forceinline__ float lse_natural(float m, float l) {
+    return l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+}
+
 __device__ __forceinline__ void set_error(const Args& a, int bits) {
     atomicOr(a.header + kHdrError, bits);
 }
@@ -176,12 +210,24 @@ __device__ __forceinline__ int64_t partial_slot(const Args& a, int g, int b, int
     return (int64_t)gl * ((int64_t)groups * a.bs + a.num_ctas) + (int64_t)grp * a.bs + b + c;
 }
 
+// Streams of the tile stream (kv-head groups; MLA: row blocks, one per draft
+// index) and the workers that split it (CTAs; MLA: 2-CTA clusters).
+__host__ __device__ __forceinline__ int stream_count(const Args& a) { return a.mla ? a.max_draft : a.hkv / a.hg; }
+__host__ __device__ __forceinline__ int worker_count(const Args& a) { return a.mla ? a.num_ctas / 2 : a.num_ctas; }
+
+// Quotient of non-negative p and positive d, in 32-bit arithmetic when both
+// fit (the usual case: a 64-bit division is a long instruction sequence).
+__device__ __forceinline__ int64_t div_nonneg(int64_t p, int64_t d) {
+    if (((uint64_t)p | (uint64_t)d) <= 0xffffffffull) return (int64_t)((uint32_t)p / (uint32_t)d);
+    return p / d;
+}
+
 // First stream tile of persistent CTA c: floor(c * W / N).
-__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t w, int n) { return (c * w) / n; }
+__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t w, int n) { return div_nonneg(c * w, n); }
 
 // The CTA whose range holds stream tile x: max{c : floor(c W / N) <= x}.
 __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t w, int n) {
-    int64_t c = ((x + 1) * n - 1) / w;
+    int64_t c = div_nonneg((x + 1) * n - 1, w);
     return c < n - 1 ? (int)c : n - 1;
 }
 

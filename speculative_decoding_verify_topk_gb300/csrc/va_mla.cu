@@ -187,6 +187,25 @@ __device__ __forceinline__ int64_t mla_slot(const Args& a, int rb, int b, int p,
     return (int64_t)rb * (a.bs + pairs) + b + p;
 }
 
+// This thread's row of O (TMEM lane address t_row, this rank's v half) times
+// inv, as bf16 output. Out of line: inlined into the softmax loop it changed
+// that loop's register allocation and slowed every tile by about 4 %.
+__device__ __noinline__ void store_final_half(uint32_t t_row, float inv, __nv_bfloat16* og) {
+    uint32_t r[32];
+#pragma unroll 1
+    for (int c = 0; c < kV / 2; c += 32) {
+        VA_TC_LD32(t_row + c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+            *reinterpret_cast<uint4*>(og + c + j) =
+                make_uint4(pack2<__nv_bfloat16>(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv),
+                           pack2<__nv_bfloat16>(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv),
+                           pack2<__nv_bfloat16>(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv),
+                           pack2<__nv_bfloat16>(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv));
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                       Args a, MlaGeo geo) {
@@ -477,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_cur = -INFINITY, l_ex = 0.f, l_rd = 0.f;
             SeqInfo si = {};
             int seg = -1;
+            bool seg_whole = false;   // the segment began at the pair's first tile
             // this rank's v-half rows of tokens past the sequence end may hold
             // garbage: zero them (0 * NaN would poison P V)
             auto zero_v_tail = [&](int st, int j0, int seq_end) {
@@ -503,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_cur = -INFINITY;
                     l_ex = l_rd = 0.f;
                     ++seg;
+                    seg_whole = cur.t == 0;
                     // 0. this row's query chunks 0..5 into TMEM once the previous
                     //    segment's score MMAs (both ranks) are done with them
                     if (seg >= 1) wait_fast(b_qfree, (seg - 1) & 1, 0, abort_flag, hdr);
@@ -671,21 +692,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_fast(b_pvdone, k & 1, 11, abort_flag, hdr);
                     fence_after();
                     const float inv = lt_rd > 0.f ? a.v_scale / lt_rd : 0.f;   // times the V dequant scale
-                    const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
-                    float* po = a.part_o + (slot * kRows + row) * kV + rank * (kV / 2);
                     uint32_t r[32];
+                    if (seg_whole && cur.t == cur.tiles - 1) {
+                        // this cluster covered the (row block, sequence) alone: the
+                        // final rows of a live block (bf16, natural-log lse)
+                        if (i < si.draft) {
+                            const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + row;
+                            store_final_half(t_o + lane_off, inv,
+                                             static_cast<__nv_bfloat16*>(a.out) + qrow * kV + rank * (kV / 2));
+                            if (rank == 0) a.lse[qrow] = lse_natural(m_cur, lt_ex);
+                        }
+                    } else {
+                        const int64_t slot = mla_slot(a, i, cur.b, blockIdx.x >> 1, geo.pairs);
+                        float* po = a.part_o + (slot * kRows + row) * kV + rank * (kV / 2);
 #pragma unroll 1
-                    for (int c = 0; c < kV / 2; c += 32) {
-                        VA_TC_LD32(t_o + c + lane_off, r);
-                        tmem_wait_ld();
+                        for (int c = 0; c < kV / 2; c += 32) {
+                            VA_TC_LD32(t_o + c + lane_off, r);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(po + c + j) =
-                                make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
-                                            __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(po + c + j) =
+                                    make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
+                                                __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+                        }
+                        if (rank == 0)
+                            a.part_lse[slot * kRows + row] = lt_ex > 0.f ? m_cur + __log2f(lt_ex) : -INFINITY;
                     }
-                    if (rank == 0)
-                        a.part_lse[slot * kRows + row] = lt_ex > 0.f ? m_cur + __log2f(lt_ex) : -INFINITY;
                     fence_before();
                 }
                 if (k + 1 < n_tiles) cur.advance(a);

@@ -19,10 +19,17 @@
 //          exclusive scan of the page counts (kv_indptr_pages), in chunks of
 //          1024 sequences with a carried total; it also (re)writes the error
 //          word, so the word describes this call only;
-//   fill   grid (bs, Y): each thread takes tokens of one sequence, checks that
-//          every slot lies on its row of the same page as the first token of
-//          its logical page, and the first token of each page writes
-//          page_table[kv_indptr_pages[b] + j / page_size].
+//   fill   a fixed grid of 4 CTAs per SM striding over the batch's tokens as
+//          one flat range kv_indptr_tok[0] .. kv_indptr_tok[bs] (a thread finds
+//          the sequence that owns its token by binary search over
+//          kv_indptr_tok), so one 64k-token sequence in a batch of short ones
+//          spreads over every SM; each thread checks that its slot lies on its
+//          row of the same page as the first token of its logical page, and
+//          the first token of each page writes
+//          page_table[kv_indptr_pages[b] + j / page_size]. When the scan found
+//          a bad length the token ranges may overlap or run backwards, and the
+//          fill walks the sequences one by one instead (a CTA per sequence,
+//          grid-strided), which is exact for any kv_indptr_tok.
 // HBM-bound: it reads every token index once (4 B per token; the page's first
 // index is re-read from L1/L2) and writes 4 B per page.
 #include <cuda_runtime.h>
@@ -111,28 +118,71 @@ __global__ void __launch_bounds__(kScanThreads)
     }
 }
 
+// Checks token j (slot kv_indices[off + j]) of a sequence whose pages start at
+// page_table[pg0]; writes the page entry when j opens a page. Returns whether
+// the slot breaks the layout.
+__device__ __forceinline__ bool fill_token(const int32_t* __restrict__ kv_indices, int64_t off, int j,
+                                           int64_t pg0, int page_size, int64_t pool_slots, int row_stride,
+                                           int64_t capacity, int32_t* __restrict__ page_table) {
+    const int r = j % page_size;
+    const int64_t slot = __ldg(kv_indices + off + j);
+    const int64_t first = r == 0 ? slot : (int64_t)__ldg(kv_indices + off + j - r);
+    const bool in_range = slot >= 0 && slot < pool_slots;
+    const bool first_in = first >= 0 && first < pool_slots;
+    const bool bad = !in_range || !first_in || slot % page_size != r || slot / page_size != first / page_size;
+    if (r == 0) {
+        const int k = j / page_size;
+        const int64_t pos = pg0 + k;
+        if ((row_stride == 0 || k < row_stride) && pos < capacity)
+            page_table[pos] = in_range ? (int32_t)(slot / page_size) : -1;
+    }
+    return bad;
+}
+
+// The last b in [0, bs) with indptr[b] <= t, for a non-decreasing indptr with
+// indptr[0] <= t < indptr[bs]: the sequence whose tokens include t (empty
+// sequences share their start with the next one and are skipped).
+__device__ __forceinline__ int owner_of(const int32_t* __restrict__ indptr, int bs, int64_t t) {
+    int lo = 0, hi = bs - 1;
+    while (lo < hi) {
+        const int mid = lo + ((hi - lo + 1) >> 1);
+        if ((int64_t)__ldg(indptr + mid) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 __global__ void __launch_bounds__(kFillThreads)
     pt_fill_kernel(const int32_t* __restrict__ tok_indptr, const int32_t* __restrict__ kv_indices,
-                   const int32_t* __restrict__ page_indptr, int page_size, int64_t pool_slots, int row_stride,
-                   int64_t capacity, int32_t* __restrict__ page_table, int32_t* __restrict__ error_word) {
-    const int b = blockIdx.x;
-    const int64_t off = __ldg(tok_indptr + b);
-    const int n = (int)(__ldg(tok_indptr + b + 1) - off);   // < 0: flagged by the scan, nothing to do
-    va::pdl_wait();   // kv_indptr_pages and the cleared error word come from the scan kernel
-    const int64_t pg0 = __ldcg(page_indptr + b);
+                   const int32_t* __restrict__ page_indptr, int bs, int page_size, int64_t pool_slots,
+                   int row_stride, int64_t capacity, int32_t* __restrict__ page_table,
+                   int32_t* __restrict__ error_word) {
+    va::pdl_wait();   // kv_indptr_pages and this call's error word come from the scan kernel
     bool bad = false;
-    for (int j = blockIdx.y * kFillThreads + threadIdx.x; j < n; j += gridDim.y * kFillThreads) {
-        const int r = j % page_size;
-        const int64_t slot = __ldg(kv_indices + off + j);
-        const int64_t first = r == 0 ? slot : (int64_t)__ldg(kv_indices + off + j - r);
-        const bool in_range = slot >= 0 && slot < pool_slots;
-        const bool first_in = first >= 0 && first < pool_slots;
-        if (!in_range || !first_in || slot % page_size != r || slot / page_size != first / page_size) bad = true;
-        if (r == 0) {
-            const int k = j / page_size;
-            if (row_stride > 0 && k >= row_stride) continue;
-            const int64_t pos = pg0 + k;
-            if (pos < capacity) page_table[pos] = in_range ? (int32_t)(slot / page_size) : -1;
+    if (!(__ldcg(error_word) & VA_ERR_BAD_LENGTH)) {
+        // kv_indptr_tok is non-decreasing: one flat range of tokens
+        const int64_t t_end = __ldg(tok_indptr + bs);
+        const int64_t stride = (int64_t)gridDim.x * kFillThreads;
+        int64_t b_beg = 0, b_end = INT64_MIN, pg0 = 0;
+        for (int64_t t = __ldg(tok_indptr) + (int64_t)blockIdx.x * kFillThreads + threadIdx.x; t < t_end;
+             t += stride) {
+            if (t >= b_end) {
+                const int b = owner_of(tok_indptr, bs, t);
+                b_beg = __ldg(tok_indptr + b);
+                b_end = __ldg(tok_indptr + b + 1);
+                pg0 = __ldcg(page_indptr + b);
+            }
+            bad |= fill_token(kv_indices, b_beg, (int)(t - b_beg), pg0, page_size, pool_slots, row_stride,
+                              capacity, page_table);
+        }
+    } else {
+        for (int b = blockIdx.x; b < bs; b += gridDim.x) {
+            const int64_t off = __ldg(tok_indptr + b);
+            const int n = (int)(__ldg(tok_indptr + b + 1) - off);   // < 0: flagged by the scan, empty
+            const int64_t pg0 = __ldcg(page_indptr + b);
+            for (int j = threadIdx.x; j < n; j += kFillThreads)
+                bad |= fill_token(kv_indices, off, j, pg0, page_size, pool_slots, row_stride, capacity,
+                                  page_table);
         }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(error_word, VA_ERR_BAD_PAGE);
@@ -147,7 +197,7 @@ extern "C" int verify_attn_build_page_table(int bs, int page_size, int64_t num_p
                                             int32_t* seq_lens, int32_t* error_word, void* stream) {
     if (bs < 0 || page_size < 1 || num_pages < 1 || capacity < 0 || row_stride < 0 || !kv_indptr_tok ||
         !kv_indices || !kv_indptr_pages || !page_table || !error_word || (seq_lens && !num_draft) ||
-        (int64_t)bs * row_stride > INT32_MAX || bs >= 65536 * 1024)
+        (int64_t)bs * row_stride > INT32_MAX)
         return VA_INVALID_ARG;
     if (bs == 0) return VA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -158,13 +208,10 @@ extern "C" int verify_attn_build_page_table(int bs, int page_size, int64_t num_p
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaGetLastError();
-    // enough CTAs for two waves over the SMs, at least one per sequence
-    int y = (2 * sms + bs - 1) / bs;
-    if (y > 64) y = 64;
-    if (y < 1) y = 1;
-    e = va::launch_pdl(pt_fill_kernel, dim3(bs, y), dim3(kFillThreads), 0, s, kv_indptr_tok, kv_indices,
-                       (const int32_t*)kv_indptr_pages, page_size, num_pages * (int64_t)page_size, row_stride,
-                       capacity, page_table, error_word);
+    // 4 CTAs of 256 threads per SM: the token count is known only on the device
+    e = va::launch_pdl(pt_fill_kernel, dim3(4 * sms), dim3(kFillThreads), 0, s, kv_indptr_tok, kv_indices,
+                       (const int32_t*)kv_indptr_pages, bs, page_size, num_pages * (int64_t)page_size,
+                       row_stride, capacity, page_table, error_word);
     if (e != cudaSuccess) return va::record_cuda_failure("page-table fill launch", e);
     return VA_OK;
 }

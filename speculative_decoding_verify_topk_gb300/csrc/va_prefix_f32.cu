@@ -62,12 +62,14 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
     cur.seek(a, x_begin, total_tiles);
     SeqInfo si = {};
     int rows_b = 0;
+    bool seg_whole = false;   // the segment began at the pair's first tile
     for (int k = 0; k < n_tiles; ++k) {
         const bool seg_begin = (k == 0) || (cur.t == 0);
         const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
         if (seg_begin) {
             si = a.seq[cur.b];
             rows_b = a.group * si.draft;
+            seg_whole = cur.t == 0;
         }
         const int j0 = si.a0 + cur.t * kTile;
         // physical rows of this tile's tokens
@@ -168,14 +170,25 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
         }
 
         if (seg_end) {
+            // the final rows when this CTA covered the (kv-head, sequence)
+            // alone, else a partial for the combine
+            const bool whole = seg_whole && cur.t == cur.tiles - 1;
             const int64_t slot = partial_slot(a, cur.g, cur.b, cta);
             for (int r = warp; r < rows_b; r += kWarps) {
                 const float l = ls[r];
                 const float inv = l > 0.f ? a.v_scale / l : 0.f;   // times the V dequantisation scale
-                float* po = a.part_o + ((int64_t)slot * a.rows_cap + r) * dv;
-                for (int d = lane; d < dv; d += 32) po[d] = os[r * dv + d] * inv;
-                if (lane == 0)
-                    a.part_lse[(int64_t)slot * a.rows_cap + r] = l > 0.f ? ms[r] + __log2f(l) : -INFINITY;
+                if (whole) {
+                    const int i = r / a.group, hh = r % a.group;
+                    const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + cur.g * a.group + hh;
+                    float* og = reinterpret_cast<float*>(a.out) + qrow * dv;
+                    for (int d = lane; d < dv; d += 32) og[d] = os[r * dv + d] * inv;
+                    if (lane == 0) a.lse[qrow] = lse_natural(ms[r], l);
+                } else {
+                    float* po = a.part_o + ((int64_t)slot * a.rows_cap + r) * dv;
+                    for (int d = lane; d < dv; d += 32) po[d] = os[r * dv + d] * inv;
+                    if (lane == 0)
+                        a.part_lse[(int64_t)slot * a.rows_cap + r] = l > 0.f ? ms[r] + __log2f(l) : -INFINITY;
+                }
             }
         }
         __syncthreads();

@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
         int rows_b = 0, lo_r[2] = {0, 0}, hi_r[2] = {0, 0};
         uint32_t tm_r[2] = {0u, 0u};   // tree verify: the rows' draft masks
+        bool seg_whole = false;        // the segment began at the pair's first tile
         SeqInfo si = {};
         auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
             if (*(volatile int*)&abort_flag) return;
@@ -320,6 +321,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             if (seg_begin) {
                 si = a.seq[cur.b];
                 rows_b = a.group * si.draft;
+                seg_whole = cur.t == 0;   // and, at its end, t == tiles - 1
                 if constexpr (QS) {
                     // the warp's 16 rows into its query area (zeros past rows_b)
                     __syncwarp();   // the previous segment's ldmatrix reads are done
@@ -562,25 +564,44 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
                 }
                 const int r0 = lane >> 2, c0 = 2 * (lane & 3);
-                // normalised partial output, times the V dequantisation scale
+                // normalised output, times the V dequantisation scale
                 const float inv0 = l_run[0] > 0.f ? a.v_scale / l_run[0] : 0.f;
                 const float inv1 = l_run[1] > 0.f ? a.v_scale / l_run[1] : 0.f;
-                const int64_t slot = partial_slot(a, g, cur.b, cta);
                 const int rr0 = wm * 16 + r0, rr1 = rr0 + 8;
-                float* po = a.part_o + (int64_t)slot * a.rows_cap * DV;
+                if (seg_whole && cur.t == cur.tiles - 1) {
+                    // this CTA covered the (kv-head, sequence) alone: the final
+                    // rows (output type, natural-log lse), no partial
 #pragma unroll
-                for (int n = 0; n < DV / 8; ++n) {
-                    if (rr0 < rows_b)
-                        *reinterpret_cast<float2*>(po + (int64_t)rr0 * DV + n * 8 + c0) =
-                            make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                    if (rr1 < rows_b)
-                        *reinterpret_cast<float2*>(po + (int64_t)rr1 * DV + n * 8 + c0) =
-                            make_float2(o[n][2] * inv1, o[n][3] * inv1);
-                }
-                if ((lane & 3) == 0) {
-                    float* pl = a.part_lse + (int64_t)slot * a.rows_cap;
-                    if (rr0 < rows_b) pl[rr0] = l_run[0] > 0.f ? m_run[0] + __log2f(l_run[0]) : -INFINITY;
-                    if (rr1 < rows_b) pl[rr1] = l_run[1] > 0.f ? m_run[1] + __log2f(l_run[1]) : -INFINITY;
+                    for (int h = 0; h < 2; ++h) {
+                        const int rr = h ? rr1 : rr0;
+                        if (rr >= rows_b) continue;
+                        const float inv = h ? inv1 : inv0;
+                        const int i = rr / a.group, hh = rr - i * a.group;
+                        const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + g * a.group + hh;
+                        T* og = reinterpret_cast<T*>(a.out) + qrow * DV + c0;
+#pragma unroll
+                        for (int n = 0; n < DV / 8; ++n)
+                            *reinterpret_cast<uint32_t*>(og + n * 8) =
+                                pack2<T>(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+                        if ((lane & 3) == 0) a.lse[qrow] = lse_natural(m_run[h], l_run[h]);
+                    }
+                } else {
+                    const int64_t slot = partial_slot(a, g, cur.b, cta);
+                    float* po = a.part_o + (int64_t)slot * a.rows_cap * DV;
+#pragma unroll
+                    for (int n = 0; n < DV / 8; ++n) {
+                        if (rr0 < rows_b)
+                            *reinterpret_cast<float2*>(po + (int64_t)rr0 * DV + n * 8 + c0) =
+                                make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                        if (rr1 < rows_b)
+                            *reinterpret_cast<float2*>(po + (int64_t)rr1 * DV + n * 8 + c0) =
+                                make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                    }
+                    if ((lane & 3) == 0) {
+                        float* pl = a.part_lse + (int64_t)slot * a.rows_cap;
+                        if (rr0 < rows_b) pl[rr0] = l_run[0] > 0.f ? m_run[0] + __log2f(l_run[0]) : -INFINITY;
+                        if (rr1 < rows_b) pl[rr1] = l_run[1] > 0.f ? m_run[1] + __log2f(l_run[1]) : -INFINITY;
+                    }
                 }
             }
             if (k + 1 < n_tiles) cur.advance(a);

@@ -76,17 +76,6 @@ struct Layout {
     static_assert(kColQ + DQK / 2 <= kTmemCols, "S, O and the query must fit in TMEM");
 };
 
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float x, float y) {
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-        return *reinterpret_cast<uint32_t*>(&h);
-    } else {
-        __half2 h = __floats2half2_rn(x, y);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-}
-
 template <typename T, int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -507,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (rows_live)
-                            a.lse[qrow] = l_sum > 0.f ? (m_ref + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+                            a.lse[qrow] = lse_natural(m_ref, l_sum);
                     } else if (wlive) {
                         const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;
                         const int64_t slot = partial_slot(a, g, cur.b, cta);

@@ -75,6 +75,38 @@ def test_builder_matches_oracle(bs, ps, max_len, seed):
     assert_same(run_builder(indptr, slots, ps, num_pages, num_draft=drafts), ref)
 
 
+@pytest.mark.parametrize("row_stride", [0, 4400])
+def test_builder_one_long_sequence_among_short_ones(row_stride):
+    """The fill spreads a batch's tokens over the whole grid: a 70,000-token
+    sequence among 128 short ones, token indices starting past element 0 of
+    kv_indices (kv_indptr_tok[0] = 37), and a slot off its row in the long one."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 41, size=129)
+    lens[77] = 70000
+    ps = 16
+    n_pages = (lens + ps - 1) // ps
+    num_pages = int(n_pages.sum()) + 500
+    perm = rng.permutation(num_pages)
+    lead = 37
+    indptr = np.concatenate([[0], np.cumsum(lens)]) + lead
+    slots = [int(x) for x in rng.integers(0, num_pages * ps, size=lead)]
+    p = 0
+    for b in range(129):
+        slots += [int(perm[p + j // ps]) * ps + j % ps for j in range(int(lens[b]))]
+        p += int(n_pages[b])
+    slots = np.asarray(slots, dtype=np.int64)
+    drafts = np.minimum(rng.integers(0, 6, size=129), lens)
+    cap = None if row_stride == 0 else 129 * row_stride
+    for bad in (False, True):
+        if bad:
+            slots[indptr[77] + 65001] += 1   # row 9 of its page holds row 10
+        ref = pto.build_page_table(indptr, slots, ps, num_pages, num_draft=drafts, capacity=cap,
+                                   row_stride=row_stride)
+        assert ref["error"] == (pto.ERR_BAD_PAGE if bad else 0)
+        assert_same(run_builder(indptr, slots, ps, num_pages, num_draft=drafts, capacity=cap,
+                                row_stride=row_stride), ref)
+
+
 def test_builder_padded_rows():
     rng = np.random.default_rng(11)
     indptr, slots, drafts, num_pages = random_token_level(rng, 40, 16, 500)
