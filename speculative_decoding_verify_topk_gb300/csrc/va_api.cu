@@ -151,7 +151,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.stages = va::mla_stages();
         ctas_per_sm = 1;
     } else if (!kv8 && out.rows_cap > 32 && out.rows_cap <= 128 && va::prefix_tc_built(p.qk_dim, p.v_dim) &&
-               va::prefix_tc_page_size_ok(p.page_size) && va::prefix_tc_stages(p.qk_dim, p.v_dim) >= 2) {
+               va::prefix_tc_page_size_ok(p.page_size) && va::prefix_tc_stages(p.qk_dim, p.v_dim, out.rows_cap) >= 2) {
         // bf16 / fp16 GQA on tcgen05: one kv-head per CTA at a time, 64-token
         // tiles. Chosen above 32 query rows per kv-head, where the warp-level
         // kernel needs three or more 16-row MMA tiles per head and turns
@@ -161,7 +161,7 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.tile_tokens = 64;
         out.heads_per_cta = 1;
         out.box_tokens = va::gcd_int(p.page_size, 64);
-        out.stages = va::prefix_tc_stages(p.qk_dim, p.v_dim);
+        out.stages = va::prefix_tc_stages(p.qk_dim, p.v_dim, out.rows_cap);
         out.stage_bytes = (p.qk_dim / 64 + p.v_dim / 64) * 64 * 128;
         ctas_per_sm = 1;
     } else {

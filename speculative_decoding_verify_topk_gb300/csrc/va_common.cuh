@@ -163,7 +163,7 @@ int mla_stages();
 bool mla_page_size_ok(int page_size);
 bool prefix_mma_built(int qk_dim, int v_dim, bool kv8);
 bool prefix_tc_built(int qk_dim, int v_dim);
-int prefix_tc_stages(int qk_dim, int v_dim);
+int prefix_tc_stages(int qk_dim, int v_dim, int rows_cap);
 bool prefix_tc_page_size_ok(int page_size);
 cudaError_t launch_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, int stages,
                              int dtype, cudaStream_t s);

@@ -53,23 +53,30 @@ constexpr int kRows = 128;     // query rows per kv-head, padded (M of both MMAs
 // sub-partitions 2 and 3, which they share with the softmax warps of rows
 // 64..127 (live only for more than 64 query rows per kv-head), so the
 // instruction stream of a busy softmax warp does not starve them. Warp 1
-// issues the P V MMAs (warp 3 the score MMAs); warp 0 only helps initialise
-// shared memory.
+// issues the P V MMAs (warp 3 the score MMAs); warp 0 loads every other tile.
 constexpr int kThreads = 256;
-constexpr int kPvWarp = 1, kProducerWarp = 2, kMmaWarp = 3, kFirstSoftmaxWarp = 4;
+constexpr int kProducerWarp2 = 0, kPvWarp = 1, kProducerWarp = 2, kMmaWarp = 3, kFirstSoftmaxWarp = 4;
 constexpr int kChunkBytes = kTok * 128;   // one 64-column chunk of a tile: [64 tokens][128 B]
 
 struct TcGeo {
     int stages;       // KV ring depth
     int tb;           // tokens per TMA box: gcd(page_size, 64), a multiple of 8
     int stage_bytes;  // (Dqk / 64 + Dv / 64) chunks
+    int p_bytes;      // distance between the two P buffers (see p_bytes_for)
     int smem_bytes;
 };
+
+// The P buffers sit at the start of shared memory, p_bytes apart, each the A
+// operand of 128 rows x 128 bytes. With at most 64 query rows per kv-head the
+// MMA rows 64..127 are padding whose products land in O rows never read, so
+// their bytes may be anything readable: the buffers overlap by half (P1's
+// rows 0..63 are P0's rows 64..127, P1's rows 64..127 the ring's first 8 KB)
+// and the 16 KB saved buy another ring stage.
+constexpr int p_bytes_for(int rows_cap) { return rows_cap <= 64 ? 64 * 128 : 128 * 128; }
 
 template <int DQK, int DV>
 struct Layout {
     static constexpr int kQc = DQK / 64, kVc = DV / 64;
-    static constexpr int kPBytes = kRows * 128;               // [128 rows][64 tokens] 16-bit
     // TMEM columns: S double-buffered, O, then the query (two 16-bit values a column)
     static constexpr uint32_t kColS = 0, kColO = 2 * kTok, kColQ = kColO + DV;
     static constexpr uint32_t kTmemCols = 512;
@@ -83,9 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Layout<DQK, DV>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* const base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char* const ring = base;
-    unsigned char* const ps = ring + geo.stages * geo.stage_bytes;   // [2] P buffers
-    uint64_t* const bars = reinterpret_cast<uint64_t*>(ps + 2 * L::kPBytes);
+    unsigned char* const ps = base;                       // [2] P buffers, geo.p_bytes apart
+    unsigned char* const ring = ps + 2 * geo.p_bytes;
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(ring + geo.stages * geo.stage_bytes);
     const uint32_t b_kfull = smem_u32(bars);                 // [stages] producer arrive + tx
     const uint32_t b_kempty = b_kfull + 8 * geo.stages;      // [stages] MMA commit
     const uint32_t b_qfull = b_kempty + 8 * geo.stages;      // 128 softmax threads (query written)
@@ -138,13 +145,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         Cursor cur;
         cur.seek(a, x_begin, total_tiles);   // cur.g = kv-head
 
-        if (warp == kProducerWarp) {
-            // =================== TMA producer (one warp) ===================
-            // Lane 0 waits for the stage and posts the byte count; then lane q
-            // issues the copies of the tile's box q0 + q, so the boxes of a tile
-            // go out in parallel. Each lane reads its box's page id two tiles
-            // ahead: the page table is cold in L2 at the start of a call, and a
-            // read on the issue path held every tile for its DRAM latency.
+        if (warp == kProducerWarp || warp == kProducerWarp2) {
+            // =================== TMA producers (two warps) ===================
+            // Warp kProducerWarp loads the even tiles, warp kProducerWarp2 the
+            // odd ones, so that each warp's bookkeeping between its tiles (page
+            // ids, box ranges, barrier arithmetic) overlaps the other's copies:
+            // with one warp the copy engine idled through it. Lane 0 waits for
+            // the stage and posts the byte count; then lane q issues the copies
+            // of the tile's box q0 + q. Each lane reads its box's page id two of
+            // its tiles ahead: the page table is cold in L2 at the start of a
+            // call, and a read on the issue path held every tile for its DRAM
+            // latency.
             const int tb_log2 = __ffs(geo.tb) - 1;   // boxes are 2^tb_log2 tokens
             const uint32_t box_bytes = (uint32_t)(L::kQc + L::kVc) * geo.tb * 128;
             struct Boxes {
@@ -198,31 +209,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the combine may launch while this CTA drains its ring
                 if (k + 1 == n_tiles && lane == 0) pdl_launch_dependents();
             };
-            // two register sets, for even and odd tiles: the page read of tile
-            // k + 2 lands in the set tile k has just used, with no copies between
+            // this warp's tiles k = par, par + 2, ...; two register sets: the page
+            // read of tile k + 4 lands in the set tile k has just used
+            const int par = warp == kProducerWarp2 ? 1 : 0;
             Cursor ahead = cur;
-            Boxes b_even = resolve(ahead), b_odd = {};
-            if (n_tiles > 1) {
+            auto skip2 = [&](int k_next) {   // ahead: from tile k_next - 2 to k_next
                 ahead.advance(a);
-                b_odd = resolve(ahead);
-            }
-            for (int k = 0; k < n_tiles; k += 2) {
-                issue_tile(k, b_even);
-                if (k + 2 < n_tiles) {
-                    ahead.advance(a);
-                    b_even = resolve(ahead);
+                ahead.advance(a);
+                (void)k_next;
+            };
+            Boxes b_a = {}, b_b = {};
+            if (par < n_tiles) {
+                if (par) ahead.advance(a);
+                b_a = resolve(ahead);
+                if (par + 2 < n_tiles) {
+                    skip2(par + 2);
+                    b_b = resolve(ahead);
                 }
-                if (k + 1 < n_tiles) {
-                    issue_tile(k + 1, b_odd);
-                    if (k + 3 < n_tiles) {
-                        ahead.advance(a);
-                        b_odd = resolve(ahead);
+            }
+            for (int k = par; k < n_tiles; k += 4) {
+                issue_tile(k, b_a);
+                if (k + 4 < n_tiles) {
+                    skip2(k + 4);
+                    b_a = resolve(ahead);
+                }
+                if (k + 2 < n_tiles) {
+                    issue_tile(k + 2, b_b);
+                    if (k + 6 < n_tiles) {
+                        skip2(k + 6);
+                        b_b = resolve(ahead);
                     }
                 }
             }
             // Normally the MMAs consume every fill before the CTA ends. After an
             // abort, wait (bounded) for the last fill of each stage.
-            if (lane == 0 && *(volatile int*)&abort_flag) {
+            if (warp == kProducerWarp && lane == 0 && *(volatile int*)&abort_flag) {
                 const int k0 = n_tiles - geo.stages > 0 ? n_tiles - geo.stages : 0;
                 for (int k = k0; k < n_tiles; ++k) mbar_wait(b_kfull + 8 * (k % geo.stages), (k / geo.stages) & 1);
             }
@@ -275,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool first = (k == 0) || (cur.t == 0);
                     wait_fast(b_pfull + 8 * (k & 1), (k >> 1) & 1, 6, &abort_flag, hdr);
                     fence_after();
-                    const uint64_t pk = p_desc + (uint64_t)(((k & 1) * L::kPBytes) >> 4);
+                    const uint64_t pk = p_desc + (uint64_t)(((k & 1) * geo.p_bytes) >> 4);
                     const uint64_t v_desc =
                         sdesc(smem_u32(ring + st * geo.stage_bytes + L::kQc * kChunkBytes), kChunkBytes, 1024, 2);
 #pragma unroll
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // swizzle; row `row` = 64 tokens = 128 bytes) once the P V two
                     // tiles back has read it; fp32 row sums
                     if (k >= 2) wait_fast(b_pvdone + 8 * sb, ((k >> 1) - 1) & 1, 9, &abort_flag, hdr);
-                    unsigned char* const prow = ps + sb * L::kPBytes + row * 128;
+                    unsigned char* const prow = ps + sb * geo.p_bytes + row * 128;
                     float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {   // 16-byte chunk q: tokens 8q .. 8q + 7
@@ -539,9 +560,9 @@ int gcd_i(int x, int y) {
 }
 
 template <int DQK, int DV>
-int smem_for(int stages) {
+int smem_for(int stages, int p_bytes) {
     using L = Layout<DQK, DV>;
-    return 1024 + stages * (L::kQc + L::kVc) * kChunkBytes + 2 * L::kPBytes + 256;
+    return 1024 + 2 * p_bytes + stages * (L::kQc + L::kVc) * kChunkBytes + 256;
 }
 
 template <typename T, int DQK, int DV>
@@ -561,15 +582,16 @@ bool prefix_tc_built(int qk, int v) {
 }
 
 // KV ring depth that fits beside the query and P (0: does not fit twice).
-int prefix_tc_stages(int qk, int v) {
+int prefix_tc_stages(int qk, int v, int rows_cap) {
+    const int pb = p_bytes_for(rows_cap);
     auto fit = [](auto smem) {
         int s = 8;   // the kernel's static shared memory (1 KB with the aligned dynamic base) counts too
         while (s >= 2 && smem(s) > 227 * 1024 - 1024 - 64) --s;
         return s >= 2 ? s : 0;
     };
-    if (qk == 128 && v == 128) return fit([](int s) { return smem_for<128, 128>(s); });
-    if (qk == 192 && v == 128) return fit([](int s) { return smem_for<192, 128>(s); });
-    if (qk == 256 && v == 256) return fit([](int s) { return smem_for<256, 256>(s); });
+    if (qk == 128 && v == 128) return fit([pb](int s) { return smem_for<128, 128>(s, pb); });
+    if (qk == 192 && v == 128) return fit([pb](int s) { return smem_for<192, 128>(s, pb); });
+    if (qk == 256 && v == 256) return fit([pb](int s) { return smem_for<256, 256>(s, pb); });
     return 0;
 }
 
@@ -582,18 +604,19 @@ cudaError_t launch_prefix_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, c
     g.tb = gcd_i(a.page_size, kTok);
     const int qc = a.qk_dim / 64, vc = a.v_dim / 64;
     g.stage_bytes = (qc + vc) * kChunkBytes;
+    g.p_bytes = p_bytes_for(a.rows_cap);
     if (g.stages < 2 || g.tb < 8 || a.hg != 1 || a.rows_cap > kRows) return cudaErrorInvalidValue;
     const bool bf = dtype == VA_BF16;
     if (a.qk_dim == 128 && a.v_dim == 128) {
-        g.smem_bytes = smem_for<128, 128>(g.stages);
+        g.smem_bytes = smem_for<128, 128>(g.stages, g.p_bytes);
         return bf ? launch_t<__nv_bfloat16, 128, 128>(kmap, vmap, a, g, s) : launch_t<__half, 128, 128>(kmap, vmap, a, g, s);
     }
     if (a.qk_dim == 192 && a.v_dim == 128) {
-        g.smem_bytes = smem_for<192, 128>(g.stages);
+        g.smem_bytes = smem_for<192, 128>(g.stages, g.p_bytes);
         return bf ? launch_t<__nv_bfloat16, 192, 128>(kmap, vmap, a, g, s) : launch_t<__half, 192, 128>(kmap, vmap, a, g, s);
     }
     if (a.qk_dim == 256 && a.v_dim == 256) {
-        g.smem_bytes = smem_for<256, 256>(g.stages);
+        g.smem_bytes = smem_for<256, 256>(g.stages, g.p_bytes);
         return bf ? launch_t<__nv_bfloat16, 256, 256>(kmap, vmap, a, g, s) : launch_t<__half, 256, 256>(kmap, vmap, a, g, s);
     }
     return cudaErrorInvalidValue;
