@@ -43,7 +43,9 @@
 // a segment start, run the softmax of own tiles (read S from TMEM, mask, max,
 // exponentials, P), apply the peer's max on its tiles, rescale O in TMEM when
 // the running max moves by more than 2^8 (lazy rescaling), and write the
-// segment's normalised partial output. The output is normalised by the sum of
+// segment's normalised output: the final bf16 rows when the cluster covered
+// the (row block, sequence) alone, else a partial for the combine. The output
+// is normalised by the sum of
 // the bf16-rounded weights P V multiplies, the log-sum-exp by the exact sum.
 //
 // Work decomposition: tiles of 64 tokens; the stream runs over (row block =

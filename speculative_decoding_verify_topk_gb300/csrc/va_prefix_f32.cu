@@ -3,8 +3,9 @@
 // Same work decomposition and partial-result contract as the bf16 / fp16
 // kernel (see va_common.cuh): each persistent CTA walks its share of the tile
 // stream (the prefix and, in each sequence's last tile, the causal drafts)
-// and writes one normalised partial output plus its base-2 log-sum-exp per
-// segment. fp32 inputs keep the 1e-4 accuracy bar, so the
+// and writes per segment the final rows, when the CTA covered the (kv-head,
+// sequence) alone, or one normalised partial output plus its base-2
+// log-sum-exp. fp32 inputs keep the 1e-4 accuracy bar, so the
 // contractions run on the CUDA cores in fp32: warp w owns query rows
 // w, w + 4, ...; lanes own tokens for Q.K and output columns for P.V. Each
 // 64-token K/V tile is gathered with 16-byte cp.async into padded shared

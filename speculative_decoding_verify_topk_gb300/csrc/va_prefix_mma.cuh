@@ -26,10 +26,12 @@
 //     complete on an mbarrier's transaction count.
 //   * NC = HG * MT consumer warps, one per (head, m16 tile of rows): QK^T and
 //     PV on the tensor cores (warp-level m16n8k16, fp32 accumulate), online
-//     softmax in base 2. A warp owns its head's rows outright, so partial
-//     results need no cross-warp merge; each warp releases the stage with one
+//     softmax in base 2. A warp owns its head's rows outright, so its results
+//     need no cross-warp merge; each warp releases the stage with one
 //     arrive. Query fragments are read straight from global memory at the
-//     start of a segment (a few per CTA).
+//     start of a segment (a few per CTA). At a segment's end the warp writes
+//     its rows' final output when the CTA covered the (head group, sequence)
+//     alone, else a partial for the combine.
 //   * V rows of tokens at or past P_b + D_b may hold another sequence's data
 //     or garbage; in the tiles that reach that far each consumer zeroes its
 //     head's V rows there before P V (0 * NaN would poison the sum).
@@ -39,7 +41,7 @@
 //     with the same swizzled layout, releases the stage at once, and runs the
 //     fp16 tensor-core path on it with the query converted to fp16 at a
 //     segment start. k_scale is folded into the softmax scale and v_scale into
-//     the partial output ("Split-KV flash-decode attention ...",
+//     the segment's output ("Split-KV flash-decode attention ...",
 //     Modifications: the prefix stage applies the fp8 k_scale / v_scale
 //     dequant multipliers).
 // Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT

@@ -20,12 +20,14 @@
 //     atoms, so page sizes must be multiples of 8) into a ring of stages;
 //   * S (128 x 64 fp32) lives in TMEM, double-buffered; O (128 x Dv fp32) too;
 //     P (bf16 / fp16) goes through shared memory as the A operand of P V, with V
-//     token-major (MN-major B);
-//   * warp 2 loads (lane q issues the copies of the tile's box q), warp 3
-//     issues the MMAs (one thread, a fixed pipeline: the scores of tile k + 1,
-//     then P V of tile k), warps 4..7 run the online softmax (thread = row)
+//     token-major (MN-major B); with at most 64 query rows the two P buffers
+//     overlap by half, which buys a fifth stage at 192/128;
+//   * warps 2 and 0 load the even and odd tiles (lane q issues the copies of
+//     the tile's box q), warp 3 issues the score MMAs and warp 1 the P V MMAs
+//     (one thread each), warps 4..7 run the online softmax (thread = row)
 //     with lazy rescaling of O in TMEM (only when a row's max grows by more
-//     than 2^8) and write the segment's partial output.
+//     than 2^8) and write the segment's result: the final rows when the CTA
+//     covered the (kv-head, sequence) alone, else a partial for the combine.
 // Compared with the warp-level kernel, the contraction runs on the tcgen05
 // pipe (about four times the legacy mma throughput) and no warp holds the
 // accumulator in registers. The plan takes this kernel for 33..128 query rows
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 fence_before();
                 mbar_arrive(b_pfull + 8 * sb);
-                // segment end: the normalised partial output, times the V scale
+                // segment end: the normalised output, times the V scale
                 // (or the final rows, when the segment is the whole pair)
                 if (seg_end) {
                     wait_fast(b_pvdone + 8 * sb, (k >> 1) & 1, 11, &abort_flag, hdr);
