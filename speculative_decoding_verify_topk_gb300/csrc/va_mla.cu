@@ -32,10 +32,13 @@
 //     64-column chunks sit in TMEM columns 64..255 (an MMA reading A from TMEM
 //     issues faster than one reading it from shared memory), the last three in
 //     shared memory;
-//   * every KV tile and the shared-memory query chunks are fetched once for
-//     the pair: each rank issues half of the TMA boxes with cluster
-//     multicast, and a stage is refilled only after both ranks' P V have
-//     released it (MMA completion multicast to both).
+//   * every tile, each rank loads the four 64-column chunks of its own v
+//     half into a ring of v slots (the scores and P V both read them); the
+//     owner of a tile also loads the five chunks its scores need besides (the
+//     peer's v half and the rope chunk) into its score slot. A slot is
+//     refilled once the MMAs that read it have completed. The query's
+//     shared-memory chunks are fetched once for the pair: each rank issues
+//     half of them with cluster multicast.
 // Roles per CTA: warp 0 issues TMA; warp 1 issues the MMAs (one thread,
 // event-driven: P V of the oldest tile once its P is in place and O
 // rescaled, else the scores of the next own tile once its stage has landed);
