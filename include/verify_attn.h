@@ -58,8 +58,8 @@ enum va_path {
     VA_PATH_MMA = 2,     /* bf16 / fp16 GQA: warp-level tensor-core tiles (any page size, FP8 pools) */
     VA_PATH_MLA = 3,     /* absorbed MLA (one latent kv-head, V aliases K): tcgen05 + TMEM */
     VA_PATH_TC = 4       /* bf16 / fp16 GQA on tcgen05 + TMEM: page sizes that are multiples of 8,
-                            33 to 128 query rows per kv-head (Hq / Hkv * max_draft), head dims
-                            128/128, 192/128, 256/256; the warp-level kernel below 33 rows */
+                            17 to 128 query rows per kv-head (Hq / Hkv * max_draft), head dims
+                            128/128, 192/128, 256/256; the warp-level kernel at 16 rows or fewer */
 };
 
 /* Bits of the device error word that verify_attn_check reports. A sequence

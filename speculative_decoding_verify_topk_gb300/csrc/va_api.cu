@@ -150,13 +150,13 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
         out.heads_per_cta = 1;
         out.stages = va::mla_stages();
         ctas_per_sm = 1;
-    } else if (!kv8 && out.rows_cap > 32 && out.rows_cap <= 128 && va::prefix_tc_built(p.qk_dim, p.v_dim) &&
+    } else if (!kv8 && out.rows_cap > 16 && out.rows_cap <= 128 && va::prefix_tc_built(p.qk_dim, p.v_dim) &&
                va::prefix_tc_page_size_ok(p.page_size) && va::prefix_tc_stages(p.qk_dim, p.v_dim, out.rows_cap) >= 2) {
         // bf16 / fp16 GQA on tcgen05: one kv-head per CTA at a time, 64-token
-        // tiles. Chosen above 32 query rows per kv-head, where the warp-level
-        // kernel needs three or more 16-row MMA tiles per head and turns
-        // latency-bound; with fewer rows it streams several kv-heads per tile
-        // and keeps the lead.
+        // tiles. Chosen above 16 query rows per kv-head, where the warp-level
+        // kernel needs two or more 16-row MMA tiles per head, takes fewer
+        // kv-heads per CTA and turns latency-bound; with one 16-row tile per
+        // head it streams 8 kv-heads per tile in large boxes and keeps the lead.
         out.path = VA_PATH_TC;
         out.tile_tokens = 64;
         out.heads_per_cta = 1;

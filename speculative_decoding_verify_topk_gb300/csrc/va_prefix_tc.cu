@@ -30,9 +30,9 @@
 //     covered the (kv-head, sequence) alone, else a partial for the combine.
 // Compared with the warp-level kernel, the contraction runs on the tcgen05
 // pipe (about four times the legacy mma throughput) and no warp holds the
-// accumulator in registers. The plan takes this kernel for 33..128 query rows
+// accumulator in registers. The plan takes this kernel for 17..128 query rows
 // per kv-head (G * D: e.g. 8 q-heads x 5 drafts), where the warp-level kernel
-// needs three or more m16 tiles per head. Every wait is bounded
+// needs two or more m16 tiles per head. Every wait is bounded
 // (VA_ERR_TIMEOUT, then the kernel winds down without waiting).
 #include <cuda.h>
 #include <cudaTypedefs.h>

@@ -83,7 +83,7 @@ def test_plan_selects_paths(lib):
     assert p.workspace_bytes % 256 == 0 and p.workspace_bytes >= (
         p.off_part_o + 4 * p.num_slots * p.rows_cap * 128)
     assert _plan(dtype=va.VA_FP32, qk_dim=64, v_dim=64, num_q_heads=4, num_kv_heads=2).path == va.VA_PATH_F32
-    # more than 32 query rows per kv-head and page sizes that are multiples of 8
+    # more than 16 query rows per kv-head and page sizes that are multiples of 8
     # go to the tcgen05 kernel: one kv-head per CTA, 64-token tiles, boxes of
     # gcd(page_size, 64) tokens
     mixed = _plan(num_q_heads=64, num_kv_heads=8, qk_dim=192, v_dim=128, max_draft=5, max_bs=128,
@@ -97,9 +97,11 @@ def test_plan_selects_paths(lib):
     assert _plan(page_size=8, **wide).path == va.VA_PATH_TC and _plan(page_size=8, **wide).box_tokens == 8
     mqa = dict(num_q_heads=32, num_kv_heads=1, max_draft=4, page_size=16)   # 32 x 4 = 128 rows
     assert _plan(**mqa).rows_cap == 128 and _plan(**mqa).path == va.VA_PATH_TC
-    # 32 rows or fewer and other page sizes stay on the warp-level kernel
+    # 17..32 rows go to it as well (two or more m16 tiles per head on the
+    # warp-level kernel); 16 rows or fewer and other page sizes stay there
+    assert _plan(page_size=64, num_q_heads=32, num_kv_heads=4, max_draft=4).path == va.VA_PATH_TC   # 32 rows
+    assert _plan(page_size=16, num_q_heads=32, num_kv_heads=8, max_draft=5).path == va.VA_PATH_TC   # 20 rows
     assert _plan(page_size=64).path == va.VA_PATH_MMA                     # 4 x 4 = 16 rows
-    assert _plan(page_size=64, num_q_heads=32, num_kv_heads=4, max_draft=4).path == va.VA_PATH_MMA
     assert _plan(num_q_heads=32, num_kv_heads=1, max_draft=4).path == va.VA_PATH_MMA   # page size 4
     # more than 128 rows per kv-head has no compiled kernel (8 m16 tiles at most)
     with pytest.raises(va.VerifyAttnError):
@@ -197,8 +199,10 @@ def test_plan_head_dim_256_caps_consumer_warps(lib):
     """At v_dim 256 a warp-level CTA runs at most 4 consumer warps (each keeps
     a 16 x 256 fp32 accumulator in registers), and the query moves to shared
     memory: the ring shrinks by 16 rows x 512 bytes per consumer warp."""
-    p = _plan(qk_dim=256, v_dim=256, num_q_heads=16, num_kv_heads=2, page_size=16)
+    p = _plan(qk_dim=256, v_dim=256, num_q_heads=16, num_kv_heads=2, page_size=4)
     assert p.path == va.VA_PATH_MMA and p.variant == 2 and p.heads_per_cta == 2
+    # the same heads at page size 16 (32 rows per kv-head) take the tcgen05 kernel
+    assert _plan(qk_dim=256, v_dim=256, num_q_heads=16, num_kv_heads=2, page_size=16).path == va.VA_PATH_TC
     assert p.stages * p.stage_bytes + 4 * 16 * 512 <= 227 * 1024 - 2048
     q = _plan(qk_dim=256, v_dim=256, num_q_heads=32, num_kv_heads=8, page_size=4)
     assert q.path == va.VA_PATH_MMA and q.heads_per_cta * q.variant <= 4

@@ -1,4 +1,4 @@
-"""Parity of the tcgen05 GQA kernel (more than 32 query rows per kv-head, page
+"""Parity of the tcgen05 GQA kernel (more than 16 query rows per kv-head, page
 sizes that are multiples of 8) with the oracle, through the C ABI. Every case
 first checks that the plan does pick that kernel, so the parity claim is about
 it and not about the warp-level kernel.
@@ -83,6 +83,19 @@ def test_33_rows_odd_group():
     """11 q-heads per kv-head with 3 drafts: 33 rows, the second warp holds one."""
     wl = wide(num_q_heads=22, num_kv_heads=2, draft=("fixed", 3))
     check(synth.make_batch(wl))
+
+
+@pytest.mark.parametrize("hq,hkv,drafts,dims", [(8, 2, 5, (128, 128)), (16, 2, 4, (256, 256)),
+                                                 (17, 1, 1, (192, 128))])
+def test_17_to_32_rows(hq, hkv, drafts, dims):
+    """17..32 rows per kv-head also take this kernel: 20 rows (4 q-heads x 5
+    drafts), 32 rows at head dim 256 (8 x 4), and 17 rows (one draft, 17
+    q-heads): one softmax warp, the other three dead."""
+    qk, v = dims
+    wl = wide(num_q_heads=hq, num_kv_heads=hkv, draft=("fixed", drafts), qk_dim=qk, v_dim=v,
+              scale=qk ** -0.5)
+    check(synth.make_batch(wl))
+    check(synth.make_batch(wl), window=100)
 
 
 def test_ragged_and_empty_prefixes():
