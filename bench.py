@@ -20,9 +20,10 @@ the events) so no call starts with a warm L2. Call i uses the workload's
 window for call i. The prefix kernel is timed on its own by events recorded
 inside the call (verify_attn_paged_profiled), which gives the live roofline
 figure. `e2e` repeats the measurement through host buffers: each step copies q
-and the per-call metadata from pinned host memory, runs the call and copies
-out / lse back, all inside the events. The KV cache is resident state (it is
-a cache) and is not copied.
+and the per-call metadata from pinned host memory (packed in one buffer, one
+copy), runs the call and copies out / lse back (one buffer, one copy), all
+inside the events. The KV cache is resident state (it is a cache) and is not
+copied.
 
 The CPU leg, after the GPU timing, times the fp64 oracle on the host cores
 (all of them, and one) on a bounded sample of the call, and holds one GPU
@@ -587,32 +588,46 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
     ms_per_step = total_ms / steps
     value = job_rate(world, steps, total_ms)
 
-    # ---- end to end through host buffers
+    # ---- end to end through host buffers: the call's inputs packed in one pinned
+    # host buffer (one host-to-device copy a step), its outputs in one device
+    # buffer (one copy back), as a serving loop would stage them
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()
-        h_q, h_pt, h_ip, h_sl, h_nd = (pin(pb.q), pin(pb.page_table), pin(pb.kv_indptr),
-                                       pin(pb.seq_lens), pin(pb.num_draft))
-        d_q, d_pt, d_ip, d_sl, d_nd = (torch.empty_like(pb.q), torch.empty_like(pb.page_table),
-                                       torch.empty_like(pb.kv_indptr), torch.empty_like(pb.seq_lens),
-                                       torch.empty_like(pb.num_draft))
-        h_tm = None if call.tree is None else pin(call.tree)
-        d_tm = None if call.tree is None else torch.empty_like(call.tree)
-        h_out = torch.empty(call.out.shape, dtype=call.out.dtype, pin_memory=True)
-        h_lse = torch.empty(call.lse.shape, dtype=call.lse.dtype, pin_memory=True)
+        ins = [pb.q, pb.page_table, pb.kv_indptr, pb.seq_lens, pb.num_draft]
+        if call.tree is not None:
+            ins.append(call.tree)
+        outs = [call.out, call.lse]
+
+        def layout(tensors, align=256):
+            offs, off = [], 0
+            for t in tensors:
+                off = (off + align - 1) // align * align
+                offs.append(off)
+                off += t.numel() * t.element_size()
+            return offs, off
+
+        def views(buf, tensors, offs):
+            return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                    for t, o in zip(tensors, offs)]
+
+        in_offs, in_bytes = layout(ins)
+        out_offs, out_bytes = layout(outs)
+        h_in = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
+        for hv, t in zip(views(h_in, ins, in_offs), ins):
+            hv.copy_(t.cpu())
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        d_ins = views(d_in, ins, in_offs)
+        d_outb = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        d_out, d_lse = views(d_outb, outs, out_offs)
+        h_outb = torch.empty(out_bytes, dtype=torch.uint8, pin_memory=True)
+        h_out, _ = views(h_outb, outs, out_offs)
         e2e_steps = min(steps, 1000)
 
         def e2e_step(i):
-            d_q.copy_(h_q, non_blocking=True)
-            d_pt.copy_(h_pt, non_blocking=True)
-            d_ip.copy_(h_ip, non_blocking=True)
-            d_sl.copy_(h_sl, non_blocking=True)
-            d_nd.copy_(h_nd, non_blocking=True)
-            if d_tm is not None:
-                d_tm.copy_(h_tm, non_blocking=True)
-            call(win(i), q=d_q, pt=d_pt, ip=d_ip, sl=d_sl, nd=d_nd, tm=d_tm)
-            h_out.copy_(call.out, non_blocking=True)
-            h_lse.copy_(call.lse, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            call(win(i), q=d_ins[0], pt=d_ins[1], ip=d_ins[2], sl=d_ins[3], nd=d_ins[4],
+                 tm=d_ins[5] if len(d_ins) > 5 else None, out=d_out, lse=d_lse)
+            h_outb.copy_(d_outb, non_blocking=True)
 
         for i in range(warmup):
             flush.zero_()
@@ -628,13 +643,14 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
         torch.cuda.synchronize(dev)
         e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        # the last step's window decides the comparison: recompute it on the device path
+        call(win(e2e_steps - 1))
+        torch.cuda.synchronize(dev)
         if not torch.equal(h_out, call.out.cpu()):
             raise RuntimeError(f"{wl.name}: e2e result differs from the device result")
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pt, h_ip, h_sl, h_nd)
-                  + (() if h_tm is None else (h_tm,)))
-        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
         e2e = {"value": job_rate(world, e2e_steps, e2e_ms), "unit": "calls/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "copies_per_step": {"h2d": 1, "d2h": 1},
                "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps}
 
     pt_builder = time_page_table_builder(pb, stream, dev, flush) if builder else None
