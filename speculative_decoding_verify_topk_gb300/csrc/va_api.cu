@@ -181,10 +181,8 @@ extern "C" int verify_attn_plan(const va_problem* problem, va_plan* plan) {
                 if (p.num_kv_heads % d != 0 || d * mt > max_nc) continue;
                 const int bstr = (tb * d * 128 + 1023) / 1024 * 1024;
                 const int stg = (p.qk_dim / slice + p.v_dim / slice) * (16 / tb) * bstr;
-                // FP8: each consumer warp's fp16 copy of its head's tile (16 tokens)
-                const int staging = kv8 ? d * mt * (p.qk_dim / 64 + p.v_dim / 64) * 2048 : 0;
                 const int qsm = d * mt * va::mma_query_smem_per_warp(p.qk_dim);
-                const int n = (kSmemLimit - 2048 - staging - qsm) / stg;
+                const int n = (kSmemLimit - 2048 - qsm) / stg;
                 if (n >= want) {
                     hg = d; box_stride = bstr; stage = stg; stages = n > 8 ? 8 : n;
                     break;
@@ -370,7 +368,6 @@ int run(const va_plan* plan, int bs, const void* q, const void* k_cache, const v
         g.nhv = p.v_dim / g.slice_cols;
         g.stage_bytes = plan->stage_bytes;
         g.stages = plan->stages;
-        g.staging_bytes = kv8 ? (p.qk_dim / 64 + p.v_dim / 64) * 2048 : 0;
         g.tx_box = (uint32_t)(g.tb * g.hg * 128);
         const va::MmaLaunch fn = va::mma_launcher(p.qk_dim, p.v_dim, kv8);
         const int64_t slots = p.num_pages * p.page_size;

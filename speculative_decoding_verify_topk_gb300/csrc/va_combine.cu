@@ -189,8 +189,8 @@ __device__ __forceinline__ void merge_row(const Args& a, int W, int part, int rs
     }
     // z == 0: the row sees no key at all (tree verify over an empty prefix with
     // no draft bit set); its output is zeros and its lse -inf
-    store_row<T, VPL>(og + lane * VPL, acc, z > 0.f ? 1.f / z : 0.f);
-    if (lane == 0) *lse_out = z > 0.f ? (mx + __log2f(z)) * 0.69314718055994531f : -INFINITY;
+    store_row<T, VPL>(og + lane * VPL, acc, z != 0.f ? 1.f / z : 0.f);
+    if (lane == 0) *lse_out = z != 0.f ? (mx + __log2f(z)) * 0.69314718055994531f : -INFINITY;
 }
 
 // Blocks per SM the register budget must allow: the CTAs are short, so more

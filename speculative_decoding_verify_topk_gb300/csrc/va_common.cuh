@@ -134,7 +134,6 @@ struct Geo {
     int nhk, nhv;          // column slices of K and of V rows
     int slice_cols;        // columns per slice: 64 (16-bit pools), 128 (FP8 pools)
     int stage_bytes, stages;
-    int staging_bytes;     // FP8 pools: per consumer warp, its head's tile converted to fp16
     uint32_t tx_box;       // bytes one box delivers
 };
 
@@ -193,7 +192,7 @@ __device__ __forceinline__ uint32_t nan_word(int dtype) {
 // Base-2 log-sum-exp of a row (running max m, sum of weights l) as the
 // natural-log value the API returns; -inf for a row that saw no key.
 __device__ __forceinline__ float lse_natural(float m, float l) {
-    return l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    return l != 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
 __device__ __forceinline__ void set_error(const Args& a, int bits) {

@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float lt_ex = l_ex + pl.x, lt_rd = l_rd + pl.y;
                     wait_fast(b_pvdone, k & 1, 11, abort_flag, hdr);
                     fence_after();
-                    const float inv = lt_rd > 0.f ? a.v_scale / lt_rd : 0.f;   // times the V dequant scale
+                    const float inv = lt_rd != 0.f ? a.v_scale / lt_rd : 0.f;   // times the V dequant scale
                     uint32_t r[32];
                     if (seg_whole && cur.t == cur.tiles - 1) {
                         // this cluster covered the (row block, sequence) alone: the
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
                         }
                         if (rank == 0)
-                            a.part_lse[slot * kRows + row] = lt_ex > 0.f ? m_cur + __log2f(lt_ex) : -INFINITY;
+                            a.part_lse[slot * kRows + row] = lt_ex != 0.f ? m_cur + __log2f(lt_ex) : -INFINITY;
                     }
                     fence_before();
                 }

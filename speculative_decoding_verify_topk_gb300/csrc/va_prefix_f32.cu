@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
             const int64_t slot = partial_slot(a, cur.g, cur.b, cta);
             for (int r = warp; r < rows_b; r += kWarps) {
                 const float l = ls[r];
-                const float inv = l > 0.f ? a.v_scale / l : 0.f;   // times the V dequantisation scale
+                const float inv = l != 0.f ? a.v_scale / l : 0.f;   // times the V dequantisation scale
                 if (whole) {
                     const int i = r / a.group, hh = r % a.group;
                     const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + cur.g * a.group + hh;
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) prefix_f32_kernel(Args a) {
                     float* po = a.part_o + ((int64_t)slot * a.rows_cap + r) * dv;
                     for (int d = lane; d < dv; d += 32) po[d] = os[r * dv + d] * inv;
                     if (lane == 0)
-                        a.part_lse[(int64_t)slot * a.rows_cap + r] = l > 0.f ? ms[r] + __log2f(l) : -INFINITY;
+                        a.part_lse[(int64_t)slot * a.rows_cap + r] = l != 0.f ? ms[r] + __log2f(l) : -INFINITY;
                 }
             }
         }

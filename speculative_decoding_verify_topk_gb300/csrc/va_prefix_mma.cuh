@@ -36,13 +36,18 @@
 //     or garbage; in the tiles that reach that far each consumer zeroes its
 //     head's V rows there before P V (0 * NaN would poison the sum).
 //   * FP8 E4M3 pools (KV8): boxes carry 128 one-byte columns per 128-byte
-//     row, halving the HBM bytes. Each consumer warp converts its head's tile
-//     (every E4M3 value is exact in fp16) into a private fp16 staging area
-//     with the same swizzled layout, releases the stage at once, and runs the
-//     fp16 tensor-core path on it with the query converted to fp16 at a
-//     segment start. k_scale is folded into the softmax scale and v_scale into
-//     the segment's output ("Split-KV flash-decode attention ...",
-//     Modifications: the prefix stage applies the fp8 k_scale / v_scale
+//     row, halving the HBM bytes. Each consumer warp reads its head's bytes of
+//     the tile straight into registers (16-byte loads, in the order the fp16
+//     m16n8k16 fragments need them), releases the stage at once, and converts
+//     them to fp16 operands in registers (every E4M3 value is exact in fp16;
+//     NaN stays NaN). Keys keep their row order with the head dimension
+//     permuted (the query takes the same permutation at a segment start,
+//     converted to fp16); values are transposed by byte permutes so that a
+//     lane holds token pairs of one column, and the output columns come out
+//     permuted and are put back by the epilogue. No staging copy: the ring
+//     takes all of shared memory. k_scale is folded into the softmax scale
+//     and v_scale into the segment's output ("Split-KV flash-decode attention
+//     ...", Modifications: the prefix stage applies the fp8 k_scale / v_scale
 //     dequant multipliers).
 // Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT
 // and the CTA winds down (no further waits) instead of hanging.
@@ -113,11 +118,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Two FP8 E4M3 values (low byte first) -> two fp16 (exact).
+// Two FP8 E4M3 values (low byte first) -> two fp16 (exact, NaN kept).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     uint32_t d;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(d) : "h"(x));
     return d;
+}
+
+// FP8 pools: for the lanes with lane % 4 = t, the K fragments of 16-column
+// step kk come from one 4-byte word of a key row: columns d0 .. d0 + 3 with
+// d0 = kv8_column(t, kk) -- 32 consecutive columns per lane in each
+// 128-column slice -- bytes 0, 1 as the step's low k-pair and bytes 2, 3 as
+// its high one. q.k does not depend on the order of the columns, so the
+// query's A fragments take the same order.
+__device__ __forceinline__ int kv8_column(int t, int kk) { return (kk >> 3) * 128 + 32 * t + 4 * (kk & 7); }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 x;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(addr));
+    return x;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& x, int j) {
+    return j == 0 ? x.x : j == 1 ? x.y : j == 2 ? x.z : x.w;
 }
 
 // 3-d tiled TMA load: box at coordinates {col, token slot, head} -> shared.
@@ -165,8 +186,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
     // 1 KB alignment for the 128-byte swizzle atoms
     unsigned char* const ring =
         smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char* const staging = ring + geo.stages * geo.stage_bytes;   // KV8: nc areas
-    unsigned char* const qsmem = staging + geo.nc * geo.staging_bytes;    // QS: nc areas
+    unsigned char* const qsmem = ring + geo.stages * geo.stage_bytes;   // QS: nc areas
     unsigned char* const bars = qsmem + geo.nc * kQSmem;
     const uint32_t bar_full = smem_u32(bars);                 // [stages], count 1 (+ tx)
     const uint32_t bar_empty = bar_full + 8 * geo.stages;     // [stages], count nc
@@ -319,6 +339,21 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             const int c = t / geo.tb, rr = gl * geo.tb + (t - c * geo.tb);   // row inside the box
             return (uint32_t)(c * geo.box_stride + rr * 128 + ((ch ^ (rr & 7)) << 4));
         };
+        // FP8 pools: offsets (inside a 128-column slice of a stage) of the
+        // 16-byte chunks this lane reads every tile. K: tokens lane / 4 and
+        // lane / 4 + 8, chunks 2 (lane % 4) and 2 (lane % 4) + 1 (the columns
+        // of kv8_column); V: tokens 2 (lane % 4) + {0, 1, 8, 9}, chunk lane / 4.
+        // Each quarter-warp's K chunks land on 8 distinct bank groups.
+        const int t4 = lane & 3, g8 = lane >> 2;
+        uint32_t koff[2][2] = {{0u, 0u}, {0u, 0u}}, voff[4] = {0u, 0u, 0u, 0u};
+        if constexpr (KV8) {
+#pragma unroll
+            for (int n8 = 0; n8 < 2; ++n8)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) koff[n8][i] = rowaddr(g8 + 8 * n8, 2 * t4 + i);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) voff[i] = rowaddr(2 * t4 + (i & 1) + 8 * (i >> 1), g8);
+        }
 
         for (int k = 0; k < n_tiles; ++k) {
             const int st = k % geo.stages;
@@ -329,7 +364,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 si = a.seq[cur.b];
                 rows_b = a.group * si.draft;
                 seg_whole = cur.t == 0;   // and, at its end, t == tiles - 1
-                if constexpr (QS) {
+                if constexpr (QS && !KV8) {
                     // the warp's 16 rows into its query area (zeros past rows_b)
                     __syncwarp();   // the previous segment's ldmatrix reads are done
                     constexpr int kChunks = DQK / 8;   // 16-byte chunks per row
@@ -342,10 +377,34 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                             const int i = r / a.group, hh = r - i * a.group;
                             x = __ldg(reinterpret_cast<const uint4*>(
                                 qg + ((int64_t)(si.qoff + i) * a.hq + g * a.group + hh) * DQK) + c);
-                            x = make_uint4(to_mma_pair<T, KV8>(x.x), to_mma_pair<T, KV8>(x.y),
-                                           to_mma_pair<T, KV8>(x.z), to_mma_pair<T, KV8>(x.w));
                         }
                         *reinterpret_cast<uint4*>(qw + qchunk(rr, c)) = x;
+                    }
+                    __syncwarp();
+                } else if constexpr (QS) {
+                    // FP8 pools: the rows in the column order of the K fragments
+                    // (see kv8_column): 16-column step kk holds, for t = 0..3 and
+                    // d0 = kv8_column(t, kk), columns d0 and d0 + 2 in its first
+                    // eight and d0 + 1 and d0 + 3 in its second eight
+                    __syncwarp();
+                    constexpr int kSteps = DQK / 16;
+#pragma unroll 2
+                    for (int it = lane; it < 16 * kSteps; it += 32) {
+                        const int rr = it / kSteps, kk = it - rr * kSteps;
+                        const int r = wm * 16 + rr;
+                        uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
+                        if (r < rows_b) {
+                            const int i = r / a.group, hh = r - i * a.group;
+                            const T* qrow = qg + ((int64_t)(si.qoff + i) * a.hq + g * a.group + hh) * DQK;
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + kv8_column(t, kk)));
+                                lo[t] = to_mma_pair<T, KV8>(u.x);
+                                hi[t] = to_mma_pair<T, KV8>(u.y);
+                            }
+                        }
+                        *reinterpret_cast<uint4*>(qw + qchunk(rr, 2 * kk)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4*>(qw + qchunk(rr, 2 * kk + 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     }
                     __syncwarp();
                 }
@@ -362,8 +421,16 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                     }
 #pragma unroll
                     for (int kk = 0; kk < DQK / 16; ++kk) {
-                        qf[kk][h] = live ? to_mma_pair<T, KV8>(__ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + c2))) : 0u;
-                        qf[kk][2 + h] = live ? to_mma_pair<T, KV8>(__ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 8 + c2))) : 0u;
+                        if constexpr (KV8) {
+                            // FP8 pools: columns d0, d0 + 1 and d0 + 2, d0 + 3 (see kv8_column)
+                            const uint2 u = live ? __ldg(reinterpret_cast<const uint2*>(qrow + kv8_column(lane & 3, kk)))
+                                                 : make_uint2(0u, 0u);
+                            qf[kk][h] = to_mma_pair<T, KV8>(u.x);
+                            qf[kk][2 + h] = to_mma_pair<T, KV8>(u.y);
+                        } else {
+                            qf[kk][h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + c2)) : 0u;
+                            qf[kk][2 + h] = live ? __ldg(reinterpret_cast<const unsigned int*>(qrow + kk * 16 + 8 + c2)) : 0u;
+                        }
                     }
                 }
 #pragma unroll
@@ -383,55 +450,34 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             }
             wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
             unsigned char* const stage = ring + st * geo.stage_bytes;
-            uint32_t kbase = smem_u32(stage);
-            uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
-            uint32_t half_stride = geo.half_bytes;
+            const uint32_t kbase = smem_u32(stage);
+            const uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
             const int tile_j0 = si.a0 + cur.t * kTT;
 
             // V rows of tokens past the sequence's end: zero them (this head)
             const int seq_end = si.prefix + si.draft;
             const bool tail = tile_j0 + kTT > seq_end;
+            // FP8 pools: this lane's K chunks of the tile into registers now, its
+            // V chunks after Q K^T (then the stage goes back to the producer);
+            // zeros for tokens no query can see -- past the sequence's end or
+            // before the window's first key: their stage bytes may be another
+            // tile's leftovers
+            uint4 kr[KV8 ? DQK / 128 : 1][2][2], vr[KV8 ? DV / 128 : 1][4];
+            auto visible = [&](int tok) {
+                const int j = tile_j0 + tok;
+                return j >= si.lo && j < seq_end;
+            };
             if constexpr (KV8) {
-                // this head's K and V rows, FP8 -> fp16, into the warp's staging
-                // area: slices of 64 columns, [slice][16 tokens][128 B], the same
-                // 16-byte-chunk swizzle. Rows no query can see -- past the
-                // sequence's end, or before the window's first key -- become
-                // zeros: their stage bytes may be another tile's leftovers
-                // (boxes wholly outside the visible keys are not refilled)
-                unsigned char* const stg = staging + warp * geo.staging_bytes;
-                __syncwarp();   // the previous tile's ldmatrix reads are done
-                constexpr int kItems = kTT * (DQK + DV) / 16;   // 16-byte FP8 chunks
 #pragma unroll
-                for (int it = lane; it < kItems; it += 32) {
-                    const int t = it & (kTT - 1), c16 = it / kTT;   // token, 16-column chunk
-                    const bool is_k = c16 < DQK / 16;
-                    const int cc = is_k ? c16 : c16 - DQK / 16;     // chunk within K or V
-                    const int part = cc >> 3, c8 = cc & 7;          // 128-column slice, chunk in it
-                    const uint32_t src = smem_u32(stage) + (is_k ? 0 : geo.nhk * geo.half_bytes) +
-                                         part * geo.half_bytes + rowaddr(t, c8);
-                    uint4 x = make_uint4(0, 0, 0, 0);
-                    if (tile_j0 + t < seq_end && tile_j0 + t >= si.lo)
-                        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
-                                     : "r"(src));
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                    uint32_t h[8];
+                for (int n8 = 0; n8 < 2; ++n8) {
+                    const bool vis = visible(g8 + 8 * n8);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        h[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
-                        h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
-                    }
-                    const int col = cc * 16;                        // first column of the chunk
-                    const int sl = col >> 6, ch0 = (col & 63) >> 3; // fp16 slice, 16-byte chunk
-                    unsigned char* const drow = stg + (is_k ? 0 : (DQK / 64) * 2048) + sl * 2048 + t * 128;
-                    *reinterpret_cast<uint4*>(drow + ((ch0 ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4*>(drow + (((ch0 + 1) ^ (t & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+                    for (int p = 0; p < DQK / 128; ++p)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+                            kr[p][n8][i] = vis ? lds128(kbase + p * geo.half_bytes + koff[n8][i])
+                                               : make_uint4(0u, 0u, 0u, 0u);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * st);   // the stage is no longer read
-                kbase = smem_u32(stg);
-                vbase = kbase + (DQK / 64) * 2048;
-                half_stride = 2048;
             } else if (tail) {
                 for (int idx = lane; idx < kTT * geo.nhv * 8; idx += 32) {
                     const int t = idx / (geo.nhv * 8), rem = idx - t * geo.nhv * 8;
@@ -443,11 +489,6 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 __syncwarp();
             }
 
-            // byte offset of 16-byte chunk ch of token t inside one 64-column slice
-            auto opaddr = [&](int t, int ch) -> uint32_t {
-                if constexpr (KV8) return (uint32_t)(t * 128 + ((ch ^ (t & 7)) << 4));
-                else return rowaddr(t, ch);
-            };
             // ---- S = Q K^T over the tile's 16 tokens (two n8 tiles); even and odd
             //      k-steps accumulate separately, halving the dependent MMA chain
             float s[2][4], s2[2][4];
@@ -455,24 +496,61 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             for (int n = 0; n < 2; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s[n][e] = s2[n][e] = 0.f;
+            // A fragments from the query area: lane l addresses row (l & 7) +
+            // 8 ((l >> 3) & 1) of the 16, 8-column chunk 2 kk + (l >> 4)
+            auto query_frag = [&](int kk, uint32_t (&qa)[4]) {
+                ldsm_x4(smem_u32(qw) + qchunk(r8 + 8 * (mi & 1), 2 * kk + (mi >> 1)), qa[0], qa[1], qa[2], qa[3]);
+            };
+            if constexpr (KV8) {
+                // B fragments straight from the registers, converted (exactly;
+                // NaN stays NaN): token n8 * 8 + lane / 4, the word of step kk
+                // (see kv8_column)
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-                const int tok = (mi >> 1) * 8 + r8;
-                const int ch = (kk & 3) * 2 + (mi & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + (kk >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
-                float (&acc)[2][4] = (kk & 1) ? s2 : s;
-                if constexpr (QS) {
-                    // A fragments: lane l addresses row (l & 7) + 8 ((l >> 3) & 1) of the
-                    // 16, 8-column chunk 2 kk + (l >> 4)
-                    uint32_t qa[4];
-                    ldsm_x4(smem_u32(qw) + qchunk(r8 + 8 * (mi & 1), 2 * kk + (mi >> 1)), qa[0], qa[1],
-                            qa[2], qa[3]);
-                    Mma<MT>::run(acc[0], qa, b0, b1);
-                    Mma<MT>::run(acc[1], qa, b2, b3);
-                } else {
-                    Mma<MT>::run(acc[0], qf[kk], b0, b1);
-                    Mma<MT>::run(acc[1], qf[kk], b2, b3);
+                for (int kk = 0; kk < DQK / 16; ++kk) {
+                    float (&acc)[2][4] = (kk & 1) ? s2 : s;
+                    uint32_t b[2][2];
+#pragma unroll
+                    for (int n8 = 0; n8 < 2; ++n8) {
+                        const uint32_t w = word_of(kr[kk >> 3][n8][(kk >> 2) & 1], kk & 3);
+                        b[n8][0] = e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+                        b[n8][1] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+                    }
+                    if constexpr (QS) {
+                        uint32_t qa[4];
+                        query_frag(kk, qa);
+                        Mma<MT>::run(acc[0], qa, b[0][0], b[0][1]);
+                        Mma<MT>::run(acc[1], qa, b[1][0], b[1][1]);
+                    } else {
+                        Mma<MT>::run(acc[0], qf[kk], b[0][0], b[0][1]);
+                        Mma<MT>::run(acc[1], qf[kk], b[1][0], b[1][1]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool vis = visible(2 * t4 + (i & 1) + 8 * (i >> 1));
+#pragma unroll
+                    for (int p = 0; p < DV / 128; ++p)
+                        vr[p][i] = vis ? lds128(vbase + p * geo.half_bytes + voff[i]) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);   // the stage is no longer read
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < DQK / 16; ++kk) {
+                    const int tok = (mi >> 1) * 8 + r8;
+                    const int ch = (kk & 3) * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbase + (kk >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
+                    float (&acc)[2][4] = (kk & 1) ? s2 : s;
+                    if constexpr (QS) {
+                        uint32_t qa[4];
+                        query_frag(kk, qa);
+                        Mma<MT>::run(acc[0], qa, b0, b1);
+                        Mma<MT>::run(acc[1], qa, b2, b3);
+                    } else {
+                        Mma<MT>::run(acc[0], qf[kk], b0, b1);
+                        Mma<MT>::run(acc[1], qf[kk], b2, b3);
+                    }
                 }
             }
 #pragma unroll
@@ -546,14 +624,40 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 pa[1] = Mma<MT>::pack(s[0][2], s[0][3]);
                 pa[2] = Mma<MT>::pack(s[1][0], s[1][1]);
                 pa[3] = Mma<MT>::pack(s[1][2], s[1][3]);
-                const int tok = (mi & 1) * 8 + r8;
+                if constexpr (KV8) {
+                    // lane (g, t) holds tokens 2t, 2t + 1, 2t + 8, 2t + 9 of columns
+                    // 128 p + 16 g + 4 j + (0..3): n8 tile 16 p + 4 j + q takes its
+                    // column 16 g + 4 j + q of slice p (output columns come out
+                    // permuted; the epilogue puts them back)
 #pragma unroll
-                for (int nd = 0; nd < DV / 16; ++nd) {
-                    const int ch = (nd & 3) * 2 + (mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vbase + (nd >> 2) * half_stride + opaddr(tok, ch), b0, b1, b2, b3);
-                    Mma<MT>::run(o[2 * nd], pa, b0, b1);
-                    Mma<MT>::run(o[2 * nd + 1], pa, b2, b3);
+                    for (int p = 0; p < DV / 128; ++p)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t w0 = word_of(vr[p][0], j), w1 = word_of(vr[p][1], j);
+                            const uint32_t w8 = word_of(vr[p][2], j), w9 = word_of(vr[p][3], j);
+                            // bytes [A0, B0, A1, B1] and [A2, B2, A3, B3] of two tokens' words:
+                            // a token pair per column, converted
+                            const uint32_t x0 = __byte_perm(w0, w1, 0x5140), x1 = __byte_perm(w0, w1, 0x7362);
+                            const uint32_t y0 = __byte_perm(w8, w9, 0x5140), y1 = __byte_perm(w8, w9, 0x7362);
+                            const uint32_t lo[4] = {   // tokens (2t, 2t + 1) of columns 4j .. 4j + 3
+                                e4m3x2_to_f16x2((uint16_t)(x0 & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
+                                e4m3x2_to_f16x2((uint16_t)(x1 & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(x1 >> 16))};
+                            const uint32_t hi[4] = {   // tokens (2t + 8, 2t + 9)
+                                e4m3x2_to_f16x2((uint16_t)(y0 & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(y0 >> 16)),
+                                e4m3x2_to_f16x2((uint16_t)(y1 & 0xffffu)), e4m3x2_to_f16x2((uint16_t)(y1 >> 16))};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) Mma<MT>::run(o[16 * p + 4 * j + q], pa, lo[q], hi[q]);
+                        }
+                } else {
+                    const int tok = (mi & 1) * 8 + r8;
+#pragma unroll
+                    for (int nd = 0; nd < DV / 16; ++nd) {
+                        const int ch = (nd & 3) * 2 + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vbase + (nd >> 2) * geo.half_bytes + rowaddr(tok, ch), b0, b1, b2, b3);
+                        Mma<MT>::run(o[2 * nd], pa, b0, b1);
+                        Mma<MT>::run(o[2 * nd + 1], pa, b2, b3);
+                    }
                 }
             }
             // release the stage; zeroed rows (generic writes) are ordered before
@@ -572,8 +676,8 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 }
                 const int r0 = lane >> 2, c0 = 2 * (lane & 3);
                 // normalised output, times the V dequantisation scale
-                const float inv0 = l_run[0] > 0.f ? a.v_scale / l_run[0] : 0.f;
-                const float inv1 = l_run[1] > 0.f ? a.v_scale / l_run[1] : 0.f;
+                const float inv0 = l_run[0] != 0.f ? a.v_scale / l_run[0] : 0.f;
+                const float inv1 = l_run[1] != 0.f ? a.v_scale / l_run[1] : 0.f;
                 const int rr0 = wm * 16 + r0, rr1 = rr0 + 8;
                 if (seg_whole && cur.t == cur.tiles - 1) {
                     // this CTA covered the (kv-head, sequence) alone: the final
@@ -585,29 +689,67 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                         const float inv = h ? inv1 : inv0;
                         const int i = rr / a.group, hh = rr - i * a.group;
                         const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + g * a.group + hh;
-                        T* og = reinterpret_cast<T*>(a.out) + qrow * DV + c0;
+                        if constexpr (KV8) {
+                            // columns 128 p + 32 t + 16 e + nd sit in o[16 p + nd][2 h + e]
+                            T* og = reinterpret_cast<T*>(a.out) + qrow * DV + 32 * t4;
 #pragma unroll
-                        for (int n = 0; n < DV / 8; ++n)
-                            *reinterpret_cast<uint32_t*>(og + n * 8) =
-                                pack2<T>(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+                            for (int p = 0; p < DV / 128; ++p)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                                    for (int n0 = 0; n0 < 16; n0 += 8) {
+                                        uint32_t w[4];
+#pragma unroll
+                                        for (int u = 0; u < 4; ++u)
+                                            w[u] = pack2<T>(o[16 * p + n0 + 2 * u][2 * h + e] * inv,
+                                                            o[16 * p + n0 + 2 * u + 1][2 * h + e] * inv);
+                                        *reinterpret_cast<uint4*>(og + 128 * p + 16 * e + n0) =
+                                            make_uint4(w[0], w[1], w[2], w[3]);
+                                    }
+                        } else {
+                            T* og = reinterpret_cast<T*>(a.out) + qrow * DV + c0;
+#pragma unroll
+                            for (int n = 0; n < DV / 8; ++n)
+                                *reinterpret_cast<uint32_t*>(og + n * 8) =
+                                    pack2<T>(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+                        }
                         if ((lane & 3) == 0) a.lse[qrow] = lse_natural(m_run[h], l_run[h]);
                     }
                 } else {
                     const int64_t slot = partial_slot(a, g, cur.b, cta);
                     float* po = a.part_o + (int64_t)slot * a.rows_cap * DV;
+                    if constexpr (KV8) {
 #pragma unroll
-                    for (int n = 0; n < DV / 8; ++n) {
-                        if (rr0 < rows_b)
-                            *reinterpret_cast<float2*>(po + (int64_t)rr0 * DV + n * 8 + c0) =
-                                make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                        if (rr1 < rows_b)
-                            *reinterpret_cast<float2*>(po + (int64_t)rr1 * DV + n * 8 + c0) =
-                                make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                        for (int h = 0; h < 2; ++h) {
+                            const int rr = h ? rr1 : rr0;
+                            if (rr >= rows_b) continue;
+                            const float inv = h ? inv1 : inv0;
+                            float* prow = po + (int64_t)rr * DV + 32 * t4;
+#pragma unroll
+                            for (int p = 0; p < DV / 128; ++p)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                                    for (int n0 = 0; n0 < 16; n0 += 4)
+                                        *reinterpret_cast<float4*>(prow + 128 * p + 16 * e + n0) = make_float4(
+                                            o[16 * p + n0][2 * h + e] * inv, o[16 * p + n0 + 1][2 * h + e] * inv,
+                                            o[16 * p + n0 + 2][2 * h + e] * inv, o[16 * p + n0 + 3][2 * h + e] * inv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int n = 0; n < DV / 8; ++n) {
+                            if (rr0 < rows_b)
+                                *reinterpret_cast<float2*>(po + (int64_t)rr0 * DV + n * 8 + c0) =
+                                    make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                            if (rr1 < rows_b)
+                                *reinterpret_cast<float2*>(po + (int64_t)rr1 * DV + n * 8 + c0) =
+                                    make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                        }
                     }
                     if ((lane & 3) == 0) {
                         float* pl = a.part_lse + (int64_t)slot * a.rows_cap;
-                        if (rr0 < rows_b) pl[rr0] = l_run[0] > 0.f ? m_run[0] + __log2f(l_run[0]) : -INFINITY;
-                        if (rr1 < rows_b) pl[rr1] = l_run[1] > 0.f ? m_run[1] + __log2f(l_run[1]) : -INFINITY;
+                        if (rr0 < rows_b) pl[rr0] = l_run[0] != 0.f ? m_run[0] + __log2f(l_run[0]) : -INFINITY;
+                        if (rr1 < rows_b) pl[rr1] = l_run[1] != 0.f ? m_run[1] + __log2f(l_run[1]) : -INFINITY;
                     }
                 }
             }
@@ -621,8 +763,7 @@ template <typename T, int DQK, int DV, bool KV8 = false>
 cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args& a, const Geo& g,
                    cudaStream_t s) {
     auto kern = prefix_mma_kernel<T, DQK, DV, KV8>;
-    const int smem = 1024 + g.stages * g.stage_bytes + g.nc * g.staging_bytes +
-                     g.nc * mma_query_smem_per_warp(DQK) + 16 * g.stages;
+    const int smem = 1024 + g.stages * g.stage_bytes + g.nc * mma_query_smem_per_warp(DQK) + 16 * g.stages;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + 1) * 32), smem, s, kmap, vmap, a, g);

@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (wlive && seg_whole && cur.t == cur.tiles - 1) {
                         // this CTA covered the (kv-head, sequence) alone: the
                         // final row (output type, natural-log lse), no partial
-                        const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;
+                        const float inv = l_sum != 0.f ? a.v_scale / l_sum : 0.f;
                         const int i = row / a.group, hh = row - i * a.group;
                         const int64_t qrow = (int64_t)(si.qoff + i) * a.hq + g * a.group + hh;
                         T* og = reinterpret_cast<T*>(a.out) + qrow * DV;
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rows_live)
                             a.lse[qrow] = lse_natural(m_ref, l_sum);
                     } else if (wlive) {
-                        const float inv = l_sum > 0.f ? a.v_scale / l_sum : 0.f;
+                        const float inv = l_sum != 0.f ? a.v_scale / l_sum : 0.f;
                         const int64_t slot = partial_slot(a, g, cur.b, cta);
                         float* po = a.part_o + (slot * a.rows_cap + row) * DV;
                         uint32_t r[32];
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (rows_live)
-                            a.part_lse[slot * a.rows_cap + row] = l_sum > 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
+                            a.part_lse[slot * a.rows_cap + row] = l_sum != 0.f ? m_ref + __log2f(l_sum) : -INFINITY;
                     }
                     fence_before();
                 }

@@ -98,3 +98,49 @@ def test_scales_on_bf16_pools():
     atol, rtol, latol = tolerance(wl.dtype)
     assert_close("scaled out", out.double().cpu().numpy(), ref_o, atol, rtol)
     assert_close("scaled lse", lse.double().cpu().numpy(), ref_l, latol, 0.0)
+
+
+def test_fp8_subnormal_codes():
+    """Pools holding only E4M3 subnormals (codes +-1..7, values m * 2^-9), with
+    scales that bring them back to unit size. The fp16 operands built from them
+    are fp16 subnormals: the tensor cores must keep them, not flush them."""
+    pb = synth.make_batch(small(k_scale=64.0, v_scale=48.0))
+    g = torch.Generator().manual_seed(5)
+    for cache in (pb.k_cache, pb.v_cache):
+        b = cache.view(torch.uint8)
+        live = (b & 0x7F) != 0x7F                      # keep the NaN poison of slots no sequence owns
+        codes = torch.randint(1, 8, b.shape, generator=g, dtype=torch.uint8)
+        codes |= torch.randint(0, 2, b.shape, generator=g, dtype=torch.uint8) << 7
+        b[live] = codes[live]
+    check(pb)
+
+
+def _slot(pb, b, j):
+    page = int(pb.page_table[int(pb.kv_indptr[b]) + j // pb.page_size])
+    return page, j % pb.page_size
+
+
+def test_fp8_nan_codes_propagate():
+    """An E4M3 NaN code in a visible key makes every row of that (sequence,
+    kv-head) NaN; one in a visible value makes that output column NaN for the
+    rows of its kv-head -- what the dequantised NaN gives in the oracle. The
+    NaN poison in slots no query sees changes nothing."""
+    pb = synth.make_batch(small())
+    wl = pb.wl
+    k8, v8 = pb.k_cache.view(torch.uint8), pb.v_cache.view(torch.uint8)
+    page, row = _slot(pb, 1, int(pb.seq_lens[1]) // 2)
+    k8[page, row, 3, 41] = 0x7F
+    page, row = _slot(pb, 2, 5)
+    v8[page, row, 6, 77] = 0xFF
+    out, lse = run(pb)
+    got_o, got_l = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    ref_o, ref_l = oracle_on(pb)
+    grp = wl.num_q_heads // wl.num_kv_heads
+    assert np.isnan(ref_o).any() and np.isnan(ref_l).any()
+    assert np.array_equal(np.isnan(got_o), np.isnan(ref_o))
+    assert np.array_equal(np.isnan(got_l), np.isnan(ref_l))
+    q1 = slice(int(pb.num_draft[:1].sum()), int(pb.num_draft[:2].sum()))
+    assert np.isnan(ref_o[q1, 3 * grp:4 * grp]).all()
+    atol, rtol, latol = tolerance(wl.dtype)
+    assert_close("fp8 out", np.nan_to_num(got_o), np.nan_to_num(ref_o), atol, rtol)
+    assert_close("fp8 lse", np.nan_to_num(got_l), np.nan_to_num(ref_l), latol, 0.0)

@@ -341,3 +341,35 @@ def test_gqa_growing_scores():
         ramp = torch.linspace(0.2, 3.0, t1 - t0).view(-1, 1, 1)
         lg.k[t0:t1] = (lg.k[t0:t1].float() * ramp).to(lg.k.dtype)
     check(synth.paginate(lg))
+
+
+def _slot(pb, b, j):
+    page = int(pb.page_table[int(pb.kv_indptr[b]) + j // pb.page_size])
+    return page, j % pb.page_size
+
+
+@pytest.mark.parametrize("num_ctas", [0, 300])
+@pytest.mark.parametrize("name", ["llama8b_gqa", "mixed_serving", "tiny", "dsv3_mla"])
+def test_nan_in_a_key_or_value_every_row_sees(name, num_ctas):
+    """A NaN in a prefix key or value element reaches the output as it does in
+    the oracle: a key NaN makes every row of its (sequence, kv-head) NaN, lse
+    included; a value NaN makes its column NaN. With many CTAs the NaN
+    segments go through the combine (num_ctas 300), else mostly not."""
+    if name == "tiny":
+        wl = synth.WORKLOADS["tiny"].replace(bs=3, prefix=("uniform", 20, 90), pool_tokens=None)
+    else:
+        wl = small(name)
+    pb = synth.make_batch(wl)
+    page, row = _slot(pb, 1, int(pb.seq_lens[1]) // 2)
+    pb.k_cache[page, row, wl.num_kv_heads - 1, wl.qk_dim - 1] = float("nan")
+    if not wl.v_aliases_k:
+        page, row = _slot(pb, 2, int(pb.seq_lens[2]) // 3)
+        pb.v_cache[page, row, 0, 5] = float("nan")
+    got_o, got_l = run_gpu(pb, num_ctas=num_ctas)
+    ref_o, ref_l = oracle_on(pb)
+    assert np.isnan(ref_o).any() and np.isnan(ref_l).any()
+    assert np.array_equal(np.isnan(got_o), np.isnan(ref_o))
+    assert np.array_equal(np.isnan(got_l), np.isnan(ref_l))
+    atol, rtol, latol = tolerance(wl.dtype)
+    assert_close("out", np.nan_to_num(got_o), np.nan_to_num(ref_o), atol, rtol)
+    assert_close("lse", np.nan_to_num(got_l), np.nan_to_num(ref_l), latol, 0.0)
