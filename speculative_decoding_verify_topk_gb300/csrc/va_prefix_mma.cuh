@@ -21,9 +21,10 @@
 //     bank-conflict free (for TB >= 8). Requests are 1-16 KB: measured on
 //     GB300, 4 KB boxes stream random pages at ~4.8 TB/s where per-thread
 //     16-byte cp.async tops out near 2.9 TB/s.
-//   * One producer warp walks the tile stream, reads page-table entries two
-//     tiles ahead, and issues the boxes into a STAGES-deep ring whose stages
-//     complete on an mbarrier's transaction count.
+//   * Two producer warps walk the tile stream (even and odd tiles), read
+//     page-table entries two of their own tiles ahead, and issue the boxes
+//     into a STAGES-deep ring whose stages complete on an mbarrier's
+//     transaction count.
 //   * NC = HG * MT consumer warps, one per (head, m16 tile of rows): QK^T and
 //     PV on the tensor cores (warp-level m16n8k16, fp32 accumulate), online
 //     softmax in base 2. A warp owns its head's rows outright, so its results
@@ -170,8 +171,13 @@ __device__ __forceinline__ uint32_t to_mma_pair(uint32_t x) {
 }
 
 constexpr int kTT = 16;            // tokens per tile
-// threads of a block: up to mma_max_consumers(DV) consumer warps and the producer
-__host__ __device__ constexpr int block_threads(int dv) { return (mma_max_consumers(dv) + 1) * 32; }
+// Producer warps: tile k is issued by producer k % kProducers. One warp's
+// issue loop -- the bulk-tensor issues, which wait while the copy engine
+// works through earlier boxes, and the page-table bookkeeping -- paced the
+// FP8 kernel; two overlap them.
+constexpr int kProducers = 2;
+// threads of a block: up to mma_max_consumers(DV) consumer warps and the producers
+__host__ __device__ constexpr int block_threads(int dv) { return (mma_max_consumers(dv) + kProducers) * 32; }
 
 template <typename T, int DQK, int DV, bool KV8>
 __global__ void __launch_bounds__(block_threads(DV), 1)
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp > geo.nc) return;   // launch may round the block up
+    if (warp >= geo.nc + kProducers) return;   // launch may round the block up
 
     pdl_wait();   // the work list (seq table, total tiles) is ready from here on
 
@@ -224,17 +230,28 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
     Cursor cur;
     cur.seek(a, x_begin, total_tiles);   // cur.g is the head group
 
-    if (warp == geo.nc) {
+    if (warp >= geo.nc) {
         // =================== producer warp ===================
-        // Lane c < ppt owns page chunk c of a tile. Its page-table read for
-        // tile k + 2 is issued in iteration k and used in iteration k + 1.
-        Cursor ahead = cur;
+        // Producer par issues tiles k = par, par + P, ... (P = kProducers).
+        // Lane c < ppt owns page chunk c of a tile. The page-table reads for
+        // its tile k + 2P are issued right after tile k's loads, into the slot
+        // tile k used (two slots, the loop unrolled by two): they have two of
+        // its iterations to land and no register copy waits on them.
+        constexpr int P = kProducers;
+        const int par = warp - geo.nc;
+        struct Slot {
+            int page = -1, off = 0;   // page id, first slot offset of this lane's chunk
+            bool valid = false;
+        };
+        auto step = [&](Cursor& c) {   // P tiles on
+#pragma unroll
+            for (int i = 0; i < P; ++i) c.advance(a);
+        };
+        Cursor mine = cur;             // the tile this producer issues next
+        for (int i = 0; i < par && i + 1 < n_tiles; ++i) mine.advance(a);
+        Cursor ahead = mine;           // the tile whose page entries load next
         int cached_b = -1, s_a0 = 0, s_lo = 0, s_end = 0, s_indptr = 0;
-        int p_page = -1, p_off = 0;         // pending (tile k + 1): page id, first slot offset
-        bool p_valid = false;
-        int n_page = -1, n_off = 0;         // tile being issued (k)
-        bool n_valid = false;
-        auto start = [&]() {
+        auto fill = [&](Slot& sl) {   // the chunk of tile `ahead`, then ahead moves on
             if (ahead.b != cached_b) {
                 const SeqInfo si = a.seq[ahead.b];
                 s_a0 = si.a0; s_lo = si.lo; s_end = si.prefix + si.draft;
@@ -242,19 +259,14 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 cached_b = ahead.b;
             }
             const int jc = s_a0 + ahead.t * kTT + lane * geo.tb;   // first token of chunk `lane`
-            p_valid = lane < geo.ppt && jc < s_end && jc + geo.tb > s_lo;
-            p_off = jc % a.page_size;
-            p_page = p_valid ? __ldg(a.page_table + s_indptr + jc / a.page_size) : -1;
+            sl.valid = lane < geo.ppt && jc < s_end && jc + geo.tb > s_lo;
+            sl.off = jc % a.page_size;
+            sl.page = sl.valid ? __ldg(a.page_table + s_indptr + jc / a.page_size) : -1;
+            step(ahead);
         };
-        start();
-        n_page = p_page; n_off = p_off; n_valid = p_valid;
-        if (n_tiles > 1) {
-            ahead.advance(a);
-            start();
-        }
         const int nparts = geo.nhk + geo.nhv;
         const int n_ops = geo.ppt * nparts;
-        for (int k = 0; k < n_tiles; ++k) {
+        auto issue = [&](int k, Slot& sl) {
             const int st = k % geo.stages;
             if (k >= geo.stages && !*(volatile int*)&abort_flag &&
                 !mbar_wait(bar_empty + 8 * st, ((k / geo.stages) - 1) & 1)) {
@@ -262,8 +274,8 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 abort_flag = 1;
             }
             // chunk validity / page range, then the stage's byte count
-            bool ok = n_valid;
-            if (ok && (n_page < 0 || n_page >= a.num_pages)) {
+            bool ok = sl.valid;
+            if (ok && (sl.page < 0 || sl.page >= a.num_pages)) {
                 ok = false;
                 set_error(a, VA_ERR_BAD_PAGE);
             }
@@ -276,37 +288,38 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             for (int op0 = 0; op0 < n_ops; op0 += 32) {   // whole-warp rounds (for the shuffles)
                 const int op = op0 + lane;
                 const int c = (op < n_ops ? op : 0) / nparts;
-                const int page = __shfl_sync(0xffffffffu, n_page, c);
-                const int off = __shfl_sync(0xffffffffu, n_off, c);
+                const int page = __shfl_sync(0xffffffffu, sl.page, c);
+                const int off = __shfl_sync(0xffffffffu, sl.off, c);
                 if (op >= n_ops || !((okmask >> c) & 1u)) continue;
                 const int part = op - c * nparts;
                 const int slot = page * a.page_size + off;
                 const uint32_t dst = sbase + part * geo.half_bytes + c * geo.box_stride;
                 if (part < geo.nhk)
-                    tma_load_3d(dst, &kmap, part * geo.slice_cols, slot, cur.g * geo.hg, full);
+                    tma_load_3d(dst, &kmap, part * geo.slice_cols, slot, mine.g * geo.hg, full);
                 else
-                    tma_load_3d(dst, &vmap, (part - geo.nhk) * geo.slice_cols, slot, cur.g * geo.hg, full);
+                    tma_load_3d(dst, &vmap, (part - geo.nhk) * geo.slice_cols, slot, mine.g * geo.hg, full);
             }
             // the combine may launch once every CTA has issued its last tile's
             // loads: its CTAs then start while the ring drains (releasing it at
             // the start parked them on the SMs for the whole run, which
             // measured slower)
             if (k + 1 == n_tiles) pdl_launch_dependents();
-            if (k + 1 < n_tiles) {
-                n_page = p_page; n_off = p_off; n_valid = p_valid;
-                if (k + 2 < n_tiles) {
-                    ahead.advance(a);
-                    start();
-                }
-                cur.advance(a);
-            }
+            if (k + 2 * P < n_tiles) fill(sl);
+            if (k + P < n_tiles) step(mine);
+        };
+        Slot s0, s1;
+        if (par < n_tiles) fill(s0);
+        if (par + P < n_tiles) fill(s1);
+        for (int k = par; k < n_tiles; k += 2 * P) {
+            issue(k, s0);
+            if (k + P < n_tiles) issue(k + P, s1);
         }
         // Normally the consumers wait for every fill, so nothing is in flight
         // at exit. After an abort, wait (bounded) for the last fill of each stage.
         if (*(volatile int*)&abort_flag) {
             const int k0 = n_tiles - geo.stages > 0 ? n_tiles - geo.stages : 0;
             for (int k = k0; k < n_tiles; ++k)
-                mbar_wait(bar_full + 8 * (k % geo.stages), (k / geo.stages) & 1);
+                if (k % P == par) mbar_wait(bar_full + 8 * (k % geo.stages), (k / geo.stages) & 1);
         }
     } else {
         // =================== consumer warps ===================
@@ -766,7 +779,7 @@ cudaError_t launch(const CUtensorMap& kmap, const CUtensorMap& vmap, const Args&
     const int smem = 1024 + g.stages * g.stage_bytes + g.nc * mma_query_smem_per_warp(DQK) + 16 * g.stages;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + 1) * 32), smem, s, kmap, vmap, a, g);
+    return launch_pdl(kern, dim3(a.num_ctas), dim3((g.nc + kProducers) * 32), smem, s, kmap, vmap, a, g);
 }
 
 }  // namespace mma_path
