@@ -346,6 +346,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 // Bulk global->shared copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) that signals completion on the mbarrier's transaction count.
+// mbar_wait for a warp that has nothing else to do (a producer waiting for a
+// free stage): each try_wait may suspend the warp for up to `hint_ns` in
+// hardware rather than return at once, so the wait takes no issue slots from
+// the consumer warps sharing its scheduler. Same bound as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (ok) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         auto issue = [&](int k, Slot& sl) {
             const int st = k % geo.stages;
             if (k >= geo.stages && !*(volatile int*)&abort_flag &&
-                !mbar_wait(bar_empty + 8 * st, ((k / geo.stages) - 1) & 1)) {
+                !mbar_wait_suspend(bar_empty + 8 * st, ((k / geo.stages) - 1) & 1, 1000u)) {
                 set_error(a, VA_ERR_TIMEOUT);
                 abort_flag = 1;
             }
