@@ -266,10 +266,11 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         };
         const int nparts = geo.nhk + geo.nhv;
         const int n_ops = geo.ppt * nparts;
+        int st = par % geo.stages;            // stage of tile k, and its round's parity
+        uint32_t ph = (uint32_t)(par / geo.stages) & 1u;
         auto issue = [&](int k, Slot& sl) {
-            const int st = k % geo.stages;
             if (k >= geo.stages && !*(volatile int*)&abort_flag &&
-                !mbar_wait_suspend(bar_empty + 8 * st, ((k / geo.stages) - 1) & 1, 1000u)) {
+                !mbar_wait_suspend(bar_empty + 8 * st, ph ^ 1u, 1000u)) {
                 set_error(a, VA_ERR_TIMEOUT);
                 abort_flag = 1;
             }
@@ -306,6 +307,11 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             if (k + 1 == n_tiles) pdl_launch_dependents();
             if (k + 2 * P < n_tiles) fill(sl);
             if (k + P < n_tiles) step(mine);
+            st += P;
+            if (st >= geo.stages) {
+                st -= geo.stages;
+                ph ^= 1u;
+            }
         };
         Slot s0, s1;
         if (par < n_tiles) fill(s0);
@@ -368,8 +374,9 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
             for (int i = 0; i < 4; ++i) voff[i] = rowaddr(2 * t4 + (i & 1) + 8 * (i >> 1), g8);
         }
 
+        int st = 0;          // stage of tile k, and its round's parity
+        uint32_t ph = 0u;
         for (int k = 0; k < n_tiles; ++k) {
-            const int st = k % geo.stages;
             const bool seg_begin = (k == 0) || (cur.t == 0);
             const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
             const int g = cur.g * geo.hg + gl;   // this warp's kv-head
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                     tm_r[h] = (a.tree && r < rows_b) ? __ldg(a.tree + si.qoff + i) : 0u;
                 }
             }
-            wait_or_abort(bar_full + 8 * st, (k / geo.stages) & 1);
+            wait_or_abort(bar_full + 8 * st, ph);
             unsigned char* const stage = ring + st * geo.stage_bytes;
             const uint32_t kbase = smem_u32(stage);
             const uint32_t vbase = kbase + geo.nhk * geo.half_bytes;
@@ -767,6 +774,10 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 }
             }
             if (k + 1 < n_tiles) cur.advance(a);
+            if (++st == geo.stages) {
+                st = 0;
+                ph ^= 1u;
+            }
         }
     }
     pdl_launch_dependents();   // (again, harmless) for warps that issued no loads
