@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         int st = par % geo.stages;            // stage of tile k, and its round's parity
         uint32_t ph = (uint32_t)(par / geo.stages) & 1u;
         auto issue = [&](int k, Slot& sl) {
-            if (k >= geo.stages && !*(volatile int*)&abort_flag &&
+            if (k >= geo.stages && !mbar_try_wait(bar_empty + 8 * st, ph ^ 1u) && !*(volatile int*)&abort_flag &&
                 !mbar_wait_suspend(bar_empty + 8 * st, ph ^ 1u, 1000u)) {
                 set_error(a, VA_ERR_TIMEOUT);
                 abort_flag = 1;
@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         bool seg_whole = false;        // the segment began at the pair's first tile
         SeqInfo si = {};
         auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+            if (mbar_try_wait(bar, parity)) return;   // the common case: the stage is in
             if (*(volatile int*)&abort_flag) return;
             if (!mbar_wait(bar, parity)) {
                 set_error(a, VA_ERR_TIMEOUT);
