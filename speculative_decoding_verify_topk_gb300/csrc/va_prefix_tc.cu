@@ -186,11 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 r.page = r.q < q1 ? __ldg(a.page_table + indptr + r.j / a.page_size) : 0;
                 return r;
             };
+            // stage of this producer's next tile (k = par, par + 2, ...) and its
+            // round's parity, as running counters: no division per tile
+            int p_st = (warp == kProducerWarp2 ? 1 : 0) % geo.stages;
+            uint32_t p_ph = (uint32_t)((warp == kProducerWarp2 ? 1 : 0) / geo.stages) & 1u;
             auto issue_tile = [&](int k, const Boxes& cb) {
-                const int st = k % geo.stages;
+                const int st = p_st;
+                const uint32_t ph = p_ph;
+                if ((p_st += 2) >= geo.stages) {
+                    p_st -= geo.stages;
+                    p_ph ^= 1u;
+                }
                 if (lane == 0) {
-                    if (k >= geo.stages)
-                        wait_fast(b_kempty + 8 * st, ((k / geo.stages) - 1) & 1, 2, &abort_flag, hdr);
+                    if (k >= geo.stages) wait_fast(b_kempty + 8 * st, ph ^ 1u, 2, &abort_flag, hdr);
                     mbar_arrive_expect_tx(b_kfull + 8 * st, (uint32_t)cb.boxes * box_bytes);
                 }
                 __syncwarp();
@@ -260,13 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
                 const uint32_t id_s = idesc_f16(kRows, kTok, 0, 0, kBf16);
                 int qk_seg = -1;
+                int st = 0;           // stage of tile k, and its round's parity
+                uint32_t ph = 0u;
                 for (int k = 0; k < n_tiles && !*(volatile int*)&abort_flag; ++k) {
                     // S = Q K^T  (M 128, N 64 tokens, K = Dqk in steps of 16)
-                    const int st = k % geo.stages, sb = k & 1;
+                    const int sb = k & 1;
                     const bool seg_begin = (k == 0) || (cur.t == 0);
                     const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
                     if (seg_begin) wait_fast(b_qfull, (++qk_seg) & 1, 3, &abort_flag, hdr);
-                    wait_fast(b_kfull + 8 * st, (k / geo.stages) & 1, 4, &abort_flag, hdr);
+                    wait_fast(b_kfull + 8 * st, ph, 4, &abort_flag, hdr);
                     if (k >= 2) wait_fast(b_sfree + 8 * sb, ((k >> 1) - 1) & 1, 5, &abort_flag, hdr);
                     fence_after();
                     const uint64_t k_desc = sdesc(smem_u32(ring + st * geo.stage_bytes), 16, 1024, 2);
@@ -279,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(b_sfull + 8 * sb);
                     if (seg_end) umma_commit(b_qfree);   // the segment's query is no longer read
                     if (k + 1 < n_tiles) cur.advance(a);
+                    if (++st == geo.stages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
                 // this thread's last commits have landed before the CTA may exit
                 wait_fast(b_sfull + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, 13, &abort_flag, hdr);
@@ -292,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
                 const uint32_t id_o = idesc_f16(kRows, DV, 0, 1, kBf16);
                 const uint64_t p_desc = sdesc(smem_u32(ps), 16, 1024, 2);
+                int st = 0;           // stage of tile k
                 for (int k = 0; k < n_tiles && !*(volatile int*)&abort_flag; ++k) {
                     // O += P V  (M 128, N Dv, K 64 tokens; V token-major)
-                    const int st = k % geo.stages;
                     const bool first = (k == 0) || (cur.t == 0);
                     wait_fast(b_pfull + 8 * (k & 1), (k >> 1) & 1, 6, &abort_flag, hdr);
                     fence_after();
@@ -308,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(b_pvdone + 8 * (k & 1));
                     umma_commit(b_kempty + 8 * st);
                     if (k + 1 < n_tiles) cur.advance(a);
+                    if (++st == geo.stages) st = 0;
                 }
                 // the last commits have landed before the CTA may exit
                 wait_fast(b_pvdone + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, 12, &abort_flag, hdr);
