@@ -86,6 +86,17 @@ constexpr int kSSlotBytes = kSChunks * kChunkBytes;         // 40 KB
 constexpr int kVSlots = 3;                                  // ring of v-half slots (every tile)
 constexpr int kPBytes = kRows * kTok * 2;                   // P: [128 rows][128 B], 128-byte swizzle
 constexpr uint32_t kColS = 0, kColQ = 64, kColO = 256;      // TMEM columns
+// Shared-memory bytes for `stages` KV stages: alignment slack, Q, ring, the own
+// and the peer's P, the peer's running max and row sums, barriers and slots.
+// The kernel declares no static shared memory, so all 227 KB are available.
+constexpr int mla_smem(int stages) {
+    return 1024 + kQBytes + kSSlotBytes + stages * kVSlotBytes + 2 * kPBytes + kRows * 4 + kRows * 8 + 256;
+}
+// v-ring depth: kVSlots when it fits. A compile-time constant, so the ring
+// index and round of tile k (k % kStages, k / kStages) cost no division in
+// the issuing threads' loops.
+constexpr int kStages = mla_smem(kVSlots) <= 227 * 1024 ? kVSlots : kVSlots - 1;
+static_assert(kStages >= 2 && mla_smem(kStages) <= 227 * 1024, "MLA ring does not fit");
 struct MlaGeo {
     int stages;          // v-half ring depth
     int tb;              // tokens per TMA box: gcd(page_size, 64)
@@ -222,14 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* const qs = base;                               // query chunks 6..8 (multicast)
     unsigned char* const sslot = qs + kQBytes;                    // own tile: the five score-only chunks
     unsigned char* const vring = sslot + kSSlotBytes;             // [stages] every tile: this rank's v half
-    unsigned char* const pown = vring + geo.stages * kVSlotBytes; // P of this CTA's tiles
+    unsigned char* const pown = vring + kStages * kVSlotBytes; // P of this CTA's tiles
     unsigned char* const ppeer = pown + kPBytes;                  // P of the peer's tiles (bulk copy)
     float* const mslot = reinterpret_cast<float*>(ppeer + kPBytes);   // [128] the peer's running max
     float2* const lx = reinterpret_cast<float2*>(mslot + kRows);     // [128] the peer's row sums
     uint64_t* const bars = reinterpret_cast<uint64_t*>(lx + kRows);
     const uint32_t b_vfull = smem_u32(bars);                     // [stages] own arrive + tx
-    const uint32_t b_vempty = b_vfull + 8 * geo.stages;          // [stages] own P V commit
-    const uint32_t b_sfull = b_vempty + 8 * geo.stages;          // own arrive + tx (score-only chunks)
+    const uint32_t b_vempty = b_vfull + 8 * kStages;          // [stages] own P V commit
+    const uint32_t b_sfull = b_vempty + 8 * kStages;          // own arrive + tx (score-only chunks)
     const uint32_t b_sempty = b_sfull + 8;                       // own score MMA commit
     const uint32_t b_qfull = b_sempty + 8;                       // own arrive + tx from both ranks
     const uint32_t b_qfree = b_qfull + 8;                        // commits of both ranks (segment's scores done)
@@ -243,17 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_pready = b_mready + 8;                      // own arrive + tx of the peer's P copy
     const uint32_t b_lbar = b_pready + 8;                        // 128 peer threads (row sums stored)
     const uint32_t b_lack = b_lbar + 8;                          // 128 peer threads (row sums read)
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * geo.stages + 16);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 16);
     int* const abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Rows a tile never fills (boxes wholly outside the visible keys, queries of
     // absent drafts) must not hold NaN bit patterns: zero Q and the KV slots once.
-    for (int i = tid; i < (kQBytes + kSSlotBytes + geo.stages * kVSlotBytes) / 16; i += kThreads)
+    for (int i = tid; i < (kQBytes + kSSlotBytes + kStages * kVSlotBytes) / 16; i += kThreads)
         reinterpret_cast<uint4*>(qs)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (tid == 0) {
-        for (int s = 0; s < geo.stages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(b_vfull + 8 * s, 1);
             mbar_init(b_vempty + 8 * s, 1);
         }
@@ -302,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto chunk_addr = [&](int c, int k) -> uint32_t {
         const int vi = c - kVChunks * (int)rank;
         if (c < 2 * kVChunks && vi >= 0 && vi < kVChunks)
-            return smem_u32(vring + (k % geo.stages) * kVSlotBytes + vi * kChunkBytes);
+            return smem_u32(vring + (k % kStages) * kVSlotBytes + vi * kChunkBytes);
         const int si = c == kChunks - 1 ? kSChunks - 1 : c - kVChunks * (int)peer;
         return smem_u32(sslot + si * kChunkBytes);
     };
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int seg = -1;
             const uint32_t box_bytes = (uint32_t)geo.tb * 128;
             for (int k = 0; k < n_tiles; ++k) {
-                const int st = k % geo.stages;
+                const int st = k % kStages;
                 const bool own = (k & 1) == (int)rank;
                 const SeqInfo si = a.seq[cur.b];
                 // resolve the tile's boxes before waiting for a slot
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (o >= 1) wait_fast(b_sempty, (o - 1) & 1, 2, abort_flag, hdr);
                         mbar_arrive_expect_tx(b_sfull, nbox * kSChunks * box_bytes);
                     }
-                    if (k >= geo.stages) wait_fast(b_vempty + 8 * st, ((k / geo.stages) - 1) & 1, 3, abort_flag, hdr);
+                    if (k >= kStages) wait_fast(b_vempty + 8 * st, ((k / kStages) - 1) & 1, 3, abort_flag, hdr);
                     mbar_arrive_expect_tx(b_vfull + 8 * st, nbox * kVChunks * box_bytes);
                 }
                 __syncwarp();
@@ -407,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (pv_next < n_tiles && !*(volatile int*)abort_flag) {
                     if (pv_next < qk_next) {
                         // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
-                        const int k = pv_next, st = k % geo.stages;
+                        const int k = pv_next, st = k % kStages;
                         const bool own = (k & 1) == (int)rank;
-                        if (mbar_test(b_pvgo, k & 1) && mbar_test(b_vfull + 8 * st, (k / geo.stages) & 1) &&
+                        if (mbar_test(b_pvgo, k & 1) && mbar_test(b_vfull + 8 * st, (k / kStages) & 1) &&
                             (own || mbar_test(b_pready, (k >> 1) & 1))) {
                             const bool first = (k == 0) || (pv_cur.t == 0);
                             fence_after();
@@ -429,12 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (qk_next < n_tiles && qk_next <= pv_next + 2) {
-                        const int k = qk_next, st = k % geo.stages;
+                        const int k = qk_next, st = k % kStages;
                         const bool own = (k & 1) == (int)rank;
                         const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
                         bool issue = !own;
                         if (own && (!need_q || (mbar_test(b_qfull, qk_seg & 1) && mbar_test(b_qtmem, qk_seg & 1))) &&
-                            mbar_test(b_sfull, (k >> 1) & 1) && mbar_test(b_vfull + 8 * st, (k / geo.stages) & 1) &&
+                            mbar_test(b_sfull, (k >> 1) & 1) && mbar_test(b_vfull + 8 * st, (k / kStages) & 1) &&
                             ((k >> 1) == 0 || mbar_test(b_sfree, ((k >> 1) - 1) & 1))) {
                             fence_after();
                             // S = Q K^T  (M 128, N 64, K 576 in 36 steps of 16)
@@ -521,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool seg_begin = (k == 0) || (cur.t == 0);
                 const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
                 const bool own = (k & 1) == (int)rank;
-                const int st = k % geo.stages;
+                const int st = k % kStages;
                 const int i = cur.g;   // draft index of this row block: one causal bound for all rows
                 if (seg_begin) {
                     si = a.seq[cur.b];
@@ -659,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l_ex *= alpha;
                     l_rd *= alpha;
                     if (tail) {   // once the slot has landed
-                        wait_fast(b_vfull + 8 * st, (k / geo.stages) & 1, 5, abort_flag, hdr);
+                        wait_fast(b_vfull + 8 * st, (k / kStages) & 1, 5, abort_flag, hdr);
                         zero_v_tail(st, j0, seq_end);
                     }
                 }
@@ -775,19 +786,7 @@ int gcd_i(int x, int y) {
 
 bool mla_available() { return true; }
 
-// Shared-memory bytes for `stages` KV stages (alignment slack, Q, ring, P, barriers).
-// Shared-memory bytes for `stages` KV stages: alignment slack, Q, ring, the own
-// and the peer's P, the peer's running max and row sums, barriers and slots.
-// The kernel declares no static shared memory, so all 227 KB are available.
-static int mla_smem(int stages) {
-    return 1024 + kQBytes + kSSlotBytes + stages * kVSlotBytes + 2 * kPBytes + kRows * 4 + kRows * 8 + 256;
-}
-
-int mla_stages() {
-    int s = kVSlots;
-    while (s > 1 && mla_smem(s) > 227 * 1024) --s;
-    return s;
-}
+int mla_stages() { return kStages; }
 
 bool mla_page_size_ok(int page_size) {
     const int tb = gcd_i(page_size, kTok);
