@@ -415,13 +415,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool need_q = true;   // the next own tile is the first of its segment here
                 int idle = 0;
                 long long idle_since = 0;
-                while (pv_next < n_tiles && !*(volatile int*)abort_flag) {
+                // The barrier tests of a poll are all issued before any result is
+                // used (their latencies overlap), and the abort flag is read only
+                // after a poll that found nothing to issue: a timed-out role
+                // leaves some barrier incomplete, so an abort always shows up as
+                // an idle poll first.
+                while (pv_next < n_tiles) {
+                    if (idle != 0 && *(volatile int*)abort_flag) break;
                     if (pv_next < qk_next) {
                         // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
                         const int k = pv_next, st = k % kStages;
                         const bool own = (k & 1) == (int)rank;
-                        if (mbar_test(b_pvgo, k & 1) && mbar_test(b_vfull + 8 * st, (k / kStages) & 1) &&
-                            (own || mbar_test(b_pready, (k >> 1) & 1))) {
+                        const bool go = mbar_test(b_pvgo, k & 1);
+                        const bool v_in = mbar_test(b_vfull + 8 * st, (k / kStages) & 1);
+                        const bool p_in = mbar_test(b_pready, (k >> 1) & 1);
+                        if (go & v_in & (own | p_in)) {
                             const bool first = (k == 0) || (pv_cur.t == 0);
                             fence_after();
                             const uint64_t v_desc =
@@ -444,9 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool own = (k & 1) == (int)rank;
                         const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
                         bool issue = !own;
-                        if (own && (!need_q || (mbar_test(b_qfull, qk_seg & 1) && mbar_test(b_qtmem, qk_seg & 1))) &&
-                            mbar_test(b_sfull, (k >> 1) & 1) && mbar_test(b_vfull + 8 * st, (k / kStages) & 1) &&
-                            ((k >> 1) == 0 || mbar_test(b_sfree, ((k >> 1) - 1) & 1))) {
+                        bool ready = false;
+                        if (own) {
+                            const bool q_in = mbar_test(b_qfull, qk_seg & 1), q_tm = mbar_test(b_qtmem, qk_seg & 1);
+                            const bool s_in = mbar_test(b_sfull, (k >> 1) & 1);
+                            const bool v_in = mbar_test(b_vfull + 8 * st, (k / kStages) & 1);
+                            const bool s_free = mbar_test(b_sfree, ((k >> 1) - 1) & 1);
+                            ready = (!need_q | (q_in & q_tm)) & s_in & v_in & ((k >> 1) == 0 | s_free);
+                        }
+                        if (ready) {
                             fence_after();
                             // S = Q K^T  (M 128, N 64, K 576 in 36 steps of 16)
 #pragma unroll
