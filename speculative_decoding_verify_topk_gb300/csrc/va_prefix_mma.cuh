@@ -355,8 +355,13 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
         const T* __restrict__ qg = reinterpret_cast<const T*>(a.q);
         // byte offset of 16-byte chunk ch (0..7) of token t (0..15) of this
         // warp's head inside one 64-column half of a stage
+        // boxes hold gcd(page_size, 16) tokens, a power of two: shifts, where the
+        // 16-bit path addresses its ldmatrix rows every k-step (the FP8 path
+        // computes its offsets once, below)
+        const int tb_log2 = __ffs(geo.tb) - 1;
         auto rowaddr = [&](int t, int ch) -> uint32_t {
-            const int c = t / geo.tb, rr = gl * geo.tb + (t - c * geo.tb);   // row inside the box
+            const int c = KV8 ? t / geo.tb : t >> tb_log2;
+            const int rr = KV8 ? gl * geo.tb + (t - c * geo.tb) : (gl << tb_log2) + (t & (geo.tb - 1));   // row inside the box
             return (uint32_t)(c * geo.box_stride + rr * 128 + ((ch ^ (rr & 7)) << 4));
         };
         // FP8 pools: offsets (inside a 128-column slice of a stage) of the
