@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // call, and a read on the issue path held every tile for its DRAM
             // latency.
             const int tb_log2 = __ffs(geo.tb) - 1;   // boxes are 2^tb_log2 tokens
+            const int ps_log2 = page_log2(a.page_size);
             const uint32_t box_bytes = (uint32_t)(L::kQc + L::kVc) * geo.tb * 128;
             struct Boxes {
                 int g, boxes, q, page, j;   // kv-head, boxes of the tile, this lane's box, its page and first token
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 r.boxes = q1 - q0;
                 r.q = q0 + lane;
                 r.j = j0 + (r.q << tb_log2);
-                r.page = r.q < q1 ? __ldg(a.page_table + indptr + r.j / a.page_size) : 0;
+                r.page = r.q < q1 ? __ldg(a.page_table + indptr + page_of(r.j, a.page_size, ps_log2)) : 0;
                 return r;
             };
             // stage of this producer's next tile (k = par, par + 2, ...) and its
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int page = cb.page;
                     if (page < 0 || page >= a.num_pages) set_error(a, VA_ERR_BAD_PAGE);
                     // an out-of-range id still delivers its bytes (from page 0) so the count balances
-                    const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size + cb.j % a.page_size;
+                    const int slot = ((page < 0 || page >= a.num_pages) ? 0 : page) * a.page_size +
+                                     row_in_page(cb.j, a.page_size, ps_log2);
                     const uint32_t dst = stg + (uint32_t)(cb.q << tb_log2) * 128;
 #pragma unroll
                     for (int c = 0; c < L::kQc; ++c)
