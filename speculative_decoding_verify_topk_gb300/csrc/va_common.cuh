@@ -276,19 +276,6 @@ struct Cursor {
     }
 };
 
-// Token j's page index and row within the page. Page sizes are usually powers
-// of two: with log2 = page_log2(page_size) >= 0 these are shifts, not the
-// divisions a runtime divisor costs in a producer's per-tile loop.
-__host__ __device__ __forceinline__ int page_log2(int page_size) {
-    int l = 0;
-    while ((1 << l) < page_size) ++l;
-    return (1 << l) == page_size ? l : -1;
-}
-__device__ __forceinline__ int page_of(int j, int page_size, int log2) { return log2 >= 0 ? j >> log2 : j / page_size; }
-__device__ __forceinline__ int row_in_page(int j, int page_size, int log2) {
-    return log2 >= 0 ? j & (page_size - 1) : j % page_size;
-}
-
 // ---- PTX wrappers ---------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

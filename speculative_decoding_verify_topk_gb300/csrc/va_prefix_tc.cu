@@ -46,6 +46,20 @@
 namespace va {
 namespace {
 
+// Token j's page index and row within the page. Page sizes are usually powers
+// of two: with log2 = page_log2(page_size) >= 0 these are shifts, not the
+// divisions a runtime divisor costs in a producer's per-tile loop.
+__device__ __forceinline__ int page_log2(int page_size) {
+    int l = 0;
+    while ((1 << l) < page_size) ++l;
+    return (1 << l) == page_size ? l : -1;
+}
+__device__ __forceinline__ int page_of(int j, int page_size, int log2) { return log2 >= 0 ? j >> log2 : j / page_size; }
+__device__ __forceinline__ int row_in_page(int j, int page_size, int log2) {
+    return log2 >= 0 ? j & (page_size - 1) : j % page_size;
+}
+
+
 using namespace tc;
 
 constexpr int kTok = 64;       // tokens per tile (N of the score MMA, K of the P V MMA)
