@@ -42,6 +42,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -195,10 +196,16 @@ def measured_peaks():
 
 
 def kernel_digest(kernel: str) -> str:
+    """Hash of the kernel's sources with comments and blank lines left out (a
+    comment edit does not change the program the ncu figures were taken on)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "speculative_decoding_verify_topk_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "speculative_decoding_verify_topk_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*$", "", line).rstrip()
+            if code.strip():
+                h.update((code + "\n").encode())
     return h.hexdigest()[:16]
 
 

@@ -29,8 +29,9 @@
 //     PV on the tensor cores (warp-level m16n8k16, fp32 accumulate), online
 //     softmax in base 2. A warp owns its head's rows outright, so its results
 //     need no cross-warp merge; each warp releases the stage with one
-//     arrive. Query fragments are read straight from global memory at the
-//     start of a segment (a few per CTA). At a segment's end the warp writes
+//     arrive. Query fragments are read from global memory at the start of a
+//     segment (a few per CTA; at qk_dim 256 through a per-warp shared-memory
+//     area, read per k-step). At a segment's end the warp writes
 //     its rows' final output when the CTA covered the (head group, sequence)
 //     alone, else a partial for the combine.
 //   * V rows of tokens at or past P_b + D_b may hold another sequence's data
@@ -39,17 +40,17 @@
 //   * FP8 E4M3 pools (KV8): boxes carry 128 one-byte columns per 128-byte
 //     row, halving the HBM bytes. Each consumer warp reads its head's bytes of
 //     the tile straight into registers (16-byte loads, in the order the fp16
-//     m16n8k16 fragments need them), releases the stage at once, and converts
-//     them to fp16 operands in registers (every E4M3 value is exact in fp16;
-//     NaN stays NaN). Keys keep their row order with the head dimension
-//     permuted (the query takes the same permutation at a segment start,
-//     converted to fp16); values are transposed by byte permutes so that a
-//     lane holds token pairs of one column, and the output columns come out
-//     permuted and are put back by the epilogue. No staging copy: the ring
-//     takes all of shared memory. k_scale is folded into the softmax scale
-//     and v_scale into the segment's output ("Split-KV flash-decode attention
-//     ...", Modifications: the prefix stage applies the fp8 k_scale / v_scale
-//     dequant multipliers).
+//     m16n8k16 fragments need them: keys before the score MMAs, values after
+//     them, then the stage goes back) and converts them to fp16 operands in
+//     registers (every E4M3 value is exact in fp16; NaN stays NaN). Keys keep
+//     their row order with the head dimension permuted (the query takes the
+//     same permutation at a segment start, converted to fp16); values are
+//     transposed by byte permutes so that a lane holds token pairs of one
+//     column, and the output columns come out permuted and are put back by
+//     the epilogue. No staging copy: the ring takes all of shared memory.
+//     k_scale is folded into the softmax scale and v_scale into the segment's
+//     output ("Split-KV flash-decode attention ...", Modifications: the
+//     prefix stage applies the fp8 k_scale / v_scale dequant multipliers).
 // Every mbarrier wait is bounded; a wait that gives up flags VA_ERR_TIMEOUT
 // and the CTA winds down (no further waits) instead of hanging.
 #pragma once
