@@ -411,8 +411,8 @@ __global__ void __launch_bounds__(block_threads(DV), 1)
                 } else if constexpr (QS) {
                     // FP8 pools: the rows in the column order of the K fragments
                     // (see kv8_column): 16-column step kk holds, for t = 0..3 and
-                    // d0 = kv8_column(t, kk), columns d0 and d0 + 2 in its first
-                    // eight and d0 + 1 and d0 + 3 in its second eight
+                    // d0 = kv8_column(t, kk), columns d0 and d0 + 1 in its first
+                    // eight and d0 + 2 and d0 + 3 in its second eight
                     __syncwarp();
                     constexpr int kSteps = DQK / 16;
 #pragma unroll 2
