@@ -101,7 +101,7 @@ WORKLOADS = {
     # the micro-benchmark shape of "Split-KV flash-decode attention for EAGLE
     # target-verify (Triton backend)", Speed Tests and Profiling: one sequence,
     # 16 q-heads / 2 kv-heads, head dim 256, 4 drafts, at three context lengths
-    # (the page size is not stated there; 16 is this build's reading)
+    # (the page size is not stated there; 16 is the reading taken here)
     **{f"p3_{n // 1024}k": Workload(f"p3_{n // 1024}k", torch.bfloat16, 1, 16, 2, 256, 256, 16,
                                     ("fixed", [n]), ("fixed", 4), 5, 1.0 / math.sqrt(256))
        for n in (4096, 16384, 65536)},
