@@ -331,6 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // slots and arms the barriers; the lanes then issue the tile's
             // boxes side by side (one thread issuing them in turn left the copy
             // engine idle between boxes).
+            // The clusters of different row blocks walk the same tiles and, started
+            // together, read each KV line at the same moment. Row block g starts
+            // (g mod 4) x 1.5 us late: the walks stay a fraction of a tile apart
+            // and the tiles' reuse in L2 holds. A measured setting, not a derived
+            // one: on dsv3_mla the prefix took 434 us with no lag and 419-421 us
+            // with lags of 0.3, 0.75, 1, 1.5, 2 and 2.5 us per row block (6 us: 423
+            // us, the later blocks' tail), but 434 us again with 0.512 us.
+            {
+                const uint64_t t0 = global_ns(), lag = (uint64_t)(cur.g & 3) * 1500u;
+                while (global_ns() - t0 < lag) __nanosleep(100);
+            }
             int seg = -1;
             const uint32_t box_bytes = (uint32_t)geo.tb * 128;
             for (int k = 0; k < n_tiles; ++k) {
