@@ -16,7 +16,9 @@ under "workloads". Prints one JSON line.
 
 Timing (per workload): W untimed calls, then K calls, each bracketed by CUDA
 events on the launching stream, with a 256 MiB write between calls (outside
-the events) so no call starts with a warm L2. Call i uses the workload's
+the events) so no call starts with a warm L2, then a ~75 us spin kernel (also
+outside) so that the call's launches are enqueued before its first event. Call
+i uses the workload's
 window for call i. The prefix kernel is timed on its own by events recorded
 inside the call (verify_attn_paged_profiled), which gives the live roofline
 figure. `e2e` repeats the measurement through host buffers: each step copies q
@@ -539,6 +541,18 @@ def smi_target(dev) -> str:
     return ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(dev.index)
 
 
+# A spin kernel of this many SM cycles (about 75 us at 2 GHz) runs after each
+# step's L2 flush and before its first event: while the GPU spins, the host
+# finishes enqueueing the call, so the events time the device work and not a
+# wait for Python's launches (a short call could otherwise reach its first event
+# before its kernels were enqueued). Outside the events; the e2e pass has none.
+HOST_LEAD_CYCLES = 150_000
+
+
+def host_lead():
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
+
+
 def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) -> dict | None:
     """Times one workload (K calls after W warm-up ones, window of call i =
     the workload's i-th) and returns its record (rank 0; None elsewhere)."""
@@ -573,6 +587,7 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
     with ClockSampler(smi_target(dev)) as clk:
         for i in range(steps):
             flush.zero_()
+            host_lead()
             ev_call[i][0].record(stream)
             call(win(i))
             ev_call[i][1].record(stream)
@@ -585,6 +600,7 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(prof_steps)]
     for i in range(prof_steps):
         flush.zero_()
+        host_lead()
         call(win(i), events=evs[i])
     torch.cuda.synchronize(dev)
     prefix_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -729,7 +745,9 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
                    "kv_tokens": int((pb.seq_lens.long() + pb.num_draft.long()).sum()),
                    "num_ctas": attn.plan.num_ctas, "tree": wl.tree,
                    "kv_dtype": str(wl.kv_type).replace("torch.", ""),
-                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "host_lead": "a 150k-cycle spin kernel after each flush, outside the events (the call is "
+                                "enqueued before its first event; not in the e2e pass)"},
         "kv_gbs": kv_gbs,
         "kv_frac_of_measured_hbm": kv_gbs / hbm_peak,
         "kv_frac_of_8tbs": kv_gbs / 8000.0,
