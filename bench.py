@@ -17,8 +17,8 @@ under "workloads". Prints one JSON line.
 Timing (per workload): W untimed calls, then K calls, each bracketed by CUDA
 events on the launching stream, with a 256 MiB write between calls (outside
 the events) so no call starts with a warm L2, then a ~75 us spin kernel (also
-outside) so that the call's launches are enqueued before its first event. Call
-i uses the workload's
+outside) so that the call's launches are enqueued before its first event;
+Python's garbage collector is off during these loops. Call i uses the workload's
 window for call i. The prefix kernel is timed on its own by events recorded
 inside the call (verify_attn_paged_profiled), which gives the live roofline
 figure. `e2e` repeats the measurement through host buffers: each step copies q
@@ -40,6 +40,7 @@ only).
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -584,6 +585,8 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
                for _ in range(steps)]
     barrier()
     torch.cuda.synchronize(dev)
+    gc.collect()
+    gc.disable()   # no collector pause between a call's first event and its launches
     with ClockSampler(smi_target(dev)) as clk:
         for i in range(steps):
             flush.zero_()
@@ -592,17 +595,20 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
             call(win(i))
             ev_call[i][1].record(stream)
         torch.cuda.synchronize(dev)
+    gc.enable()
     barrier()
     total_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev_call)
     # second pass: events recorded between the call's three kernels
     # (verify_attn_paged_profiled) time each kernel on its own stream
     prof_steps = min(steps, 500)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(prof_steps)]
+    gc.disable()
     for i in range(prof_steps):
         flush.zero_()
         host_lead()
         call(win(i), events=evs[i])
     torch.cuda.synchronize(dev)
+    gc.enable()
     prefix_ms = [e[1].elapsed_time(e[2]) for e in evs]
     combine_ms = [e[2].elapsed_time(e[3]) for e in evs]
     worklist_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -747,7 +753,8 @@ def measure(wl, args, dev, world: int, rank: int, flush, builder: bool = False) 
                    "kv_dtype": str(wl.kv_type).replace("torch.", ""),
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "host_lead": "a 150k-cycle spin kernel after each flush, outside the events (the call is "
-                                "enqueued before its first event; not in the e2e pass)"},
+                                "enqueued before its first event), and no garbage collection during the "
+                                "device-timed loops; neither in the e2e pass"},
         "kv_gbs": kv_gbs,
         "kv_frac_of_measured_hbm": kv_gbs / hbm_peak,
         "kv_frac_of_8tbs": kv_gbs / 8000.0,
