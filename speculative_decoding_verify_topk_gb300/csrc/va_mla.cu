@@ -33,13 +33,15 @@
 //     issues faster than one reading it from shared memory), the last three in
 //     shared memory;
 //   * every tile, each rank loads the four 64-column chunks of its own v
-//     half into a ring of v slots (the scores and P V both read them); the
-//     owner of a tile also loads the five chunks its scores need besides (the
-//     peer's v half and the rope chunk) into its score slot. A slot is
-//     refilled once the MMAs that read it have completed. The query's
+//     half into one of three v slots (the scores and P V both read them):
+//     its own tiles alternate between two slots, the peer's tiles use the
+//     third; the owner of a tile also loads the five chunks its scores need
+//     besides (the peer's v half and the rope chunk) into its score slot. A
+//     slot is refilled once the MMAs that read it have completed. The query's
 //     shared-memory chunks are fetched once for the pair: each rank issues
 //     half of them with cluster multicast.
-// Roles per CTA: warp 0 issues TMA; warp 1 issues the MMAs (one thread,
+// Roles per CTA: warp 0 issues TMA for the query and the own tiles, warp 6
+// for the peer's tiles; warp 1 issues the MMAs (one thread,
 // event-driven: P V of the oldest tile once its P is in place and O
 // rescaled, else the scores of the next own tile once its stage has landed);
 // warps 2..5 (128 threads, thread = row) write the TMEM part of the query at
@@ -76,7 +78,7 @@ constexpr int kQk = 576, kV = 512;
 constexpr int kChunk = 64;        // columns per 128-byte swizzle chunk
 constexpr int kChunks = kQk / kChunk;   // 9
 constexpr int kQTmem = 6;         // query chunks 0..5 in TMEM (32 columns each), 6..8 in shared memory
-constexpr int kThreads = 192;     // producer, MMA, 4 softmax warps
+constexpr int kThreads = 224;     // producer, MMA, 4 softmax warps, producer of the peer's tiles
 constexpr int kQBytes = (kChunks - kQTmem) * kRows * 128;   // [chunk][128 rows][128 B], 128-byte swizzle
 constexpr int kChunkBytes = kTok * 128;                     // one 64-column chunk of a tile: [64 tokens][128 B]
 constexpr int kVChunks = 4;                                 // a rank's v half: chunks 4 r .. 4 r + 3
@@ -96,7 +98,7 @@ constexpr int mla_smem(int stages) {
 // index and round of tile k (k % kStages, k / kStages) cost no division in
 // the issuing threads' loops.
 constexpr int kStages = mla_smem(kVSlots) <= 227 * 1024 ? kVSlots : kVSlots - 1;
-static_assert(kStages >= 2 && mla_smem(kStages) <= 227 * 1024, "MLA ring does not fit");
+static_assert(kStages == 3 && mla_smem(kStages) <= 227 * 1024, "MLA ring does not fit");
 struct MlaGeo {
     int stages;          // v-half ring depth
     int tb;              // tokens per TMA box: gcd(page_size, 64)
@@ -310,10 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* const hdr = a.header;
     // a chunk c's shared-memory home in tile k: this rank's v-half chunks in
     // the tile's v slot, the others (own tiles only) in the score slot
+    // v slot of tile k and the parity of its use. Own tiles alternate between
+    // slots 0 and 1, each freed by the P V of the own tile four back (it runs
+    // right after this rank's softmax); the peer's tiles use slot 2, freed by
+    // the P V of the peer's tile two back (it waits for the peer's P). With one
+    // ring of three, an own tile's v half waited for the peer's tile's P V.
+    auto vslot = [&](int k) -> int { return ((k & 1) == (int)rank) ? ((k >> 1) & 1) : 2; };
+    auto vphase = [&](int k) -> uint32_t { return (uint32_t)(((k & 1) == (int)rank) ? (k >> 2) : (k >> 1)) & 1u; };
+    auto vreused = [&](int k) -> bool { return ((k & 1) == (int)rank) ? k >= 4 : k >= 2; };   // slot used before
     auto chunk_addr = [&](int c, int k) -> uint32_t {
         const int vi = c - kVChunks * (int)rank;
         if (c < 2 * kVChunks && vi >= 0 && vi < kVChunks)
-            return smem_u32(vring + (k % kStages) * kVSlotBytes + vi * kChunkBytes);
+            return smem_u32(vring + vslot(k) * kVSlotBytes + vi * kChunkBytes);
         const int si = c == kChunks - 1 ? kSChunks - 1 : c - kVChunks * (int)peer;
         return smem_u32(sslot + si * kChunkBytes);
     };
@@ -322,8 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         Cursor cur;
         cur.seek(a, x_begin, total_tiles);   // cur.g = row block (draft index)
 
-        if (warp == 0) {
-            // =================== TMA producer (one warp) ===================
+        if (warp == 0 || warp == 6) {
+            // =================== TMA producers (two warps) ===================
+            // Warp 0 loads the query and the own tiles, warp 6 the v half of the
+            // peer's tiles, so that a wait for slot 2 never holds an own tile.
             // Every tile: this rank's v-half chunks into the v ring. Own tiles
             // (k % 2 == rank) also: the five score-only chunks into the score
             // slot, issued first, as soon as that slot is free (it frees about a
@@ -346,10 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (global_ns() - t0 < lag) __nanosleep(100);
             }
             int seg = -1;
+            const bool prod_own = warp == 0;   // this warp loads the own tiles (and the query)
             const uint32_t box_bytes = (uint32_t)geo.tb * 128;
             for (int k = 0; k < n_tiles; ++k) {
-                const int st = k % kStages;
+                const int st = vslot(k);
                 const bool own = (k & 1) == (int)rank;
+                const bool mine = prod_own == own;   // this warp loads tile k's KV
                 const SeqInfo si = a.seq[cur.b];
                 // resolve the tile's boxes before waiting for a slot
                 const int j0 = si.a0 + cur.t * kTok;
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < kTok / 8; ++q) {
                     const int j = j0 + q * geo.tb;
                     slot[q] = -1;
-                    if (q * geo.tb < kTok && j < end && j + geo.tb > si.lo) {   // box overlaps [lo, P + D)
+                    if (mine && q * geo.tb < kTok && j < end && j + geo.tb > si.lo) {   // box overlaps [lo, P + D)
                         const int page = __ldg(a.page_table + indptr + j / a.page_size);
                         if (lane == 0 && (page < 0 || page >= a.num_pages)) set_error(a, VA_ERR_BAD_PAGE);
                         // an out-of-range id still delivers its bytes (from page 0) so the count balances
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++nbox;
                     }
                 }
-                if (lane == 0) {
+                if (lane == 0 && prod_own) {
                     if (k == 0 || cur.t == 0) {
                         ++seg;
                         if (seg >= 1) wait_fast(b_qfree, (seg - 1) & 1, 1, abort_flag, hdr);
@@ -401,20 +415,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_2d(chunk_addr(c, k) + q * box_bytes, &kmap, c * kChunk, slot[q], b_sfull);
                     }
                 }
-                if (lane == 0) {
-                    if (k >= kStages) wait_fast(b_vempty + 8 * st, ((k / kStages) - 1) & 1, 3, abort_flag, hdr);
+                if (lane == 0 && mine) {
+                    if (vreused(k)) wait_fast(b_vempty + 8 * st, vphase(k) ^ 1u, 3, abort_flag, hdr);
                     mbar_arrive_expect_tx(b_vfull + 8 * st, nbox * kVChunks * box_bytes);
                 }
                 __syncwarp();
-                // this rank's v half (every tile)
-                for (int op = lane; op < (kTok / 8) * kVChunks; op += 32) {
+                for (int op = lane; mine && op < (kTok / 8) * kVChunks; op += 32) {
                     const int q = op / kVChunks, ci = op - q * kVChunks;
                     if (slot[q] < 0) continue;
                     const int c = kVChunks * (int)rank + ci;
                     tma_2d(chunk_addr(c, k) + q * box_bytes, &kmap, c * kChunk, slot[q], b_vfull + 8 * st);
                 }
                 // the combine may launch while this CTA drains its ring
-                if (k + 1 == n_tiles && lane == 0) pdl_launch_dependents();
+                if (k + 1 == n_tiles && lane == 0 && prod_own) pdl_launch_dependents();
                 if (k + 1 < n_tiles) cur.advance(a);
             }
         } else if (warp == 1) {
@@ -447,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (idle != 0 && *(volatile int*)abort_flag) break;
                     if (pv_next < qk_next) {
                         // O[:, half] += P V[:, half]  (M 128, N 256, K 64 tokens; V token-major)
-                        const int k = pv_next, st = k % kStages;
+                        const int k = pv_next, st = vslot(k);
                         const bool own = (k & 1) == (int)rank;
                         const bool go = mbar_test(b_pvgo, k & 1);
-                        const bool v_in = mbar_test(b_vfull + 8 * st, (k / kStages) & 1);
+                        const bool v_in = mbar_test(b_vfull + 8 * st, vphase(k));
                         const bool p_in = mbar_test(b_pready, (k >> 1) & 1);
                         if (go & v_in & (own | p_in)) {
                             const bool first = (k == 0) || (pv_cur.t == 0);
@@ -470,8 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             continue;
                         }
                     }
-                    if (qk_next < n_tiles && qk_next <= pv_next + 2) {
-                        const int k = qk_next, st = k % kStages;
+                    // the scores of tile k at most three tiles ahead of P V: P V of
+                    // tile k - 4 has been issued, so the v-slot fill an own tile
+                    // waits for is the slot's pending phase (its earlier fill, tile
+                    // k - 4's, has been taken)
+                    if (qk_next < n_tiles && qk_next <= pv_next + 3) {
+                        const int k = qk_next, st = vslot(k);
                         const bool own = (k & 1) == (int)rank;
                         const bool seg_end = (k == n_tiles - 1) || (qk_cur.t == qk_cur.tiles - 1);
                         bool issue = !own;
@@ -479,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (own) {
                             const bool q_in = mbar_test(b_qfull, qk_seg & 1), q_tm = mbar_test(b_qtmem, qk_seg & 1);
                             const bool s_in = mbar_test(b_sfull, (k >> 1) & 1);
-                            const bool v_in = mbar_test(b_vfull + 8 * st, (k / kStages) & 1);
+                            const bool v_in = mbar_test(b_vfull + 8 * st, vphase(k));
                             const bool s_free = mbar_test(b_sfree, ((k >> 1) - 1) & 1);
                             ready = (!need_q | (q_in & q_tm)) & s_in & v_in & ((k >> 1) == 0 | s_free);
                         }
@@ -533,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_fast(b_pfree + 8 * (k & 1), (k >> 1) & 1, 12, abort_flag, hdr);
                 wait_fast(b_qfree, qk_seg & 1, 13, abort_flag, hdr);
             }
-        } else {
+        } else if (warp < 6) {
             // =================== softmax warps: thread = row ===================
             const int row = (warp & 3) * 32 + lane;              // TMEM lane quadrant = warp % 4
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -569,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool seg_begin = (k == 0) || (cur.t == 0);
                 const bool seg_end = (k == n_tiles - 1) || (cur.t == cur.tiles - 1);
                 const bool own = (k & 1) == (int)rank;
-                const int st = k % kStages;
+                const int st = vslot(k);
                 const int i = cur.g;   // draft index of this row block: one causal bound for all rows
                 if (seg_begin) {
                     si = a.seq[cur.b];
@@ -707,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l_ex *= alpha;
                     l_rd *= alpha;
                     if (tail) {   // once the slot has landed
-                        wait_fast(b_vfull + 8 * st, (k / kStages) & 1, 5, abort_flag, hdr);
+                        wait_fast(b_vfull + 8 * st, vphase(k), 5, abort_flag, hdr);
                         zero_v_tail(st, j0, seq_end);
                     }
                 }
